@@ -1,0 +1,184 @@
+/*
+ * smla.h — C ABI of the GB300 (sm_103a) sparse multi-head latent attention
+ * (MLA) decode library, libsmla.so.
+ *
+ * What is computed (one decode step).  Each query row r has H heads that
+ * share one latent KV pool.  Row r attends to a multiset of entries, in this
+ * order: the valid slots of its top-k index list into the main cache, its
+ * sliding window, and its compressed-cache entries.  Each entry holds 448
+ * FP8-e4m3 NoPE dims with one UE8M0 scale per 64 dims and 64 bf16 RoPE dims;
+ * dequantised, it is a 512-wide vector x_e used as both key and value.  For
+ * head h with query q_h = [q_nope | q_rope] (512 wide):
+ *
+ *     s_e   = sm_scale * <q_h, x_e>
+ *     lse_h = ln( e^{sink_h} + sum_e e^{s_e} )        (natural log, sink included)
+ *     out_h = sum_e e^{s_e - lse_h} * x_e             (512 wide, bf16)
+ *
+ * Sources: "[ROCm][DSV4][Perf] Optimize Triton sparse-MLA decode on gfx950"
+ * (vLLM pull request 52212), section "Design": the 512-wide combined
+ * NoPE + RoPE QK dot, the 512-wide PV, guarded main/window tiles, compressed
+ * 64-entry groups with masked tails, attention sinks, invalid indices with
+ * zero probability, 64-bit block address arithmetic; and "[ASM] [HIP] [MLA v4
+ * nm] Split plan helper and persistent decode kernel with in-kernel split and
+ * merge" (ROCm/aiter pull request 6126), summary part 1 (host split planner
+ * from a cost model) and part 2 (one launch; split plan computed in the
+ * kernel from the real lengths on every call; split rows merged by the
+ * last-arriving work-group from fp32 partials plus LSE; unsplit rows write
+ * bf16 directly; CUDA-graph safe with varying lengths; the workspace is
+ * allocated outside capture and calls sharing it are stream-ordered).
+ *
+ * Threading: every function is thread-safe.  The library allocates no device
+ * memory and keeps no per-call state; the caller owns every buffer.
+ */
+#ifndef SMLA_H_
+#define SMLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque CUDA stream handle (a cudaStream_t / CUstream); NULL = legacy default stream. */
+typedef void* smla_stream_t;
+
+typedef enum smla_status {
+    SMLA_OK = 0,
+    SMLA_ERR_NULL_POINTER = 1,        /* a required pointer is NULL                    */
+    SMLA_ERR_MISALIGNED = 2,          /* a pointer breaks its stated alignment          */
+    SMLA_ERR_BAD_SHAPE = 3,           /* rows / heads / topk / splits / sizes out of range */
+    SMLA_ERR_WORKSPACE_TOO_SMALL = 4, /* ws_bytes < smla_workspace_bytes(...)           */
+    SMLA_ERR_UNSUPPORTED_DEVICE = 5,  /* current device is not compute capability 10.3  */
+    SMLA_ERR_CUDA = 6                 /* a CUDA runtime call or the launch failed       */
+} smla_status;
+
+/* Bits of the device error word (smla_read_device_error).  Bad device data
+ * never traps: the offending slot is treated as invalid (zero probability)
+ * and a bit is set. */
+#define SMLA_DEV_BAD_INDEX   0x1u  /* top-k index < -1, or a logical position that does not map into the pool */
+#define SMLA_DEV_BAD_CMP     0x2u  /* compressed range outside [0, n_cmp): the excess is dropped */
+#define SMLA_DEV_BAD_LENGTH  0x4u  /* negative swa_len / cmp_len: treated as 0 */
+#define SMLA_DEV_TIMEOUT     0x8u  /* a bounded wait inside the kernel gave up; outputs of the
+                                      call are undefined and the workspace must be re-zeroed */
+
+/* Fixed geometry of one KV entry. */
+#define SMLA_NOPE_DIMS   448
+#define SMLA_ROPE_DIMS   64
+#define SMLA_HEAD_DIM    512  /* QK width and PV width */
+#define SMLA_ENTRY_BYTES 576  /* 448 fp8 bytes followed by 64 little-endian bf16 */
+#define SMLA_SCALE_BYTES 8    /* 7 UE8M0 codes (one per 64 NoPE dims) + 1 pad byte */
+#define SMLA_PAGE_SIZE   64   /* tokens per page of block_table */
+#define SMLA_MAX_HEADS   128
+#define SMLA_MAX_ROWS    1024
+#define SMLA_MAX_SPLITS  32
+
+/*
+ * Arguments of one decode call.  All pointers are DEVICE pointers owned by
+ * the caller.  Layouts are C-contiguous.  bf16 arrays are given as raw 16-bit
+ * storage.  Required alignments: q_nope, q_rope, kv_pool, cmp_pool, out 16 B;
+ * kv_scales, cmp_scales 8 B; every int32 / float array 4 B.
+ */
+typedef struct smla_decode_args {
+    const void* q_nope;          /* bf16 [num_rows][num_heads][448]                                */
+    const void* q_rope;          /* bf16 [num_rows][num_heads][64]                                 */
+    const void* kv_pool;         /* u8   [n_main][576]: main-cache entries                          */
+    const void* kv_scales;       /* u8   [n_main][8]:   UE8M0 codes, scale = 2^(code-127)           */
+    int64_t n_main;              /* rows in kv_pool (may exceed 2^31 / 576: addressing is 64-bit)   */
+    const int32_t* block_table;  /* [num_seqs][pages_per_seq] physical page ids, or NULL: logical
+                                    position == physical row.  Position p of sequence s lives in
+                                    row block_table[s][p/64]*64 + p%64.                             */
+    int32_t pages_per_seq;       /* row stride of block_table (ignored when it is NULL)             */
+    const int32_t* row_seq;      /* [num_rows] sequence of each row, or NULL: row r reads sequence r */
+    const int32_t* main_idx;     /* [num_rows][topk] logical positions, -1 = invalid slot           */
+    int32_t topk;                /* 0 disables the top-k source (main_idx may then be NULL)          */
+    const int32_t* swa_start;    /* [num_rows] first logical position of the sliding window          */
+    const int32_t* swa_len;      /* [num_rows] window length; NULL disables the window              */
+    const void* cmp_pool;        /* u8 [n_cmp][576]: compressed-cache entries                        */
+    const void* cmp_scales;      /* u8 [n_cmp][8]                                                    */
+    int64_t n_cmp;               /* rows in cmp_pool                                                 */
+    const int32_t* cmp_start;    /* [num_rows] first compressed row of the row                       */
+    const int32_t* cmp_len;      /* [num_rows] compressed entries of the row; NULL disables them     */
+    const float* sink;           /* [num_heads] per-head sink logit (scaled domain), NULL = no sink  */
+    float sm_scale;              /* softmax scale applied to <q, x>                                  */
+    void* out;                   /* bf16 [num_rows][num_heads][512]                                  */
+    float* lse;                  /* [num_rows][num_heads] natural-log LSE incl. sink, or NULL        */
+    int32_t num_rows;            /* 1 .. SMLA_MAX_ROWS                                               */
+    int32_t num_heads;           /* 1 .. SMLA_MAX_HEADS                                              */
+    int32_t num_splits;          /* 1 .. SMLA_MAX_SPLITS: split budget per row (from the planner).
+                                    The grid holds num_rows*num_splits work units; the kernel hands
+                                    them to rows in proportion to each row's live length.  Keep it
+                                    fixed across CUDA-graph replays (it sizes the grid).            */
+} smla_decode_args;
+
+/*
+ * Host-side split planner.  Cost model (aiter pull request 6126, summary
+ * part 1): choose s in [1, SMLA_MAX_SPLITS] minimising
+ *     waves(num_rows * s) * (t0 + c_entry * ceil(kv_len / s))
+ *       + [s > 1] * (c_byte * num_rows * num_heads * 512 * 4 * s + c_merge),
+ * waves(u) = ceil(u / slots); ties go to the smaller s.  kv_len is the
+ * caller's per-row entry count (top-k slots + window + compressed entries).
+ * Pure host code: no device work, no allocation.  Returns s >= 1, or the
+ * negated smla_status (SMLA_ERR_BAD_SHAPE) for num_rows < 1, num_heads not in
+ * [1, 128] or kv_len < 0.
+ */
+int smla_plan_num_splits(int num_rows, int num_heads, int64_t kv_len);
+
+/* The planner's coefficients; the built-in set is fitted for GB300. */
+typedef struct smla_plan_coeffs {
+    double slots;    /* work units that run concurrently (one unit = one CTA pair) */
+    double t0;       /* fixed time per unit, microseconds                           */
+    double c_entry;  /* time per KV entry per unit, microseconds                    */
+    double c_byte;   /* partial write + read-back cost, microseconds per byte       */
+    double c_merge;  /* fixed merge cost of a split call, microseconds              */
+} smla_plan_coeffs;
+
+/* Copies the built-in GB300 coefficients into *out.  Returns SMLA_OK or SMLA_ERR_NULL_POINTER. */
+smla_status smla_plan_default_coeffs(smla_plan_coeffs* out);
+
+/* Same cost model with caller-supplied coefficients (NULL = built-in) and an
+ * upper bound s_max in [1, SMLA_MAX_SPLITS].  Same return convention. */
+int smla_plan_num_splits_ex(int num_rows, int num_heads, int64_t kv_len,
+                            const smla_plan_coeffs* coeffs, int s_max);
+
+/*
+ * Workspace bytes for calls with up to max_rows rows, num_heads heads and a
+ * split budget of max_splits (cf. the persistent kernel's workspace getter in
+ * aiter pull request 6126, summary part 2).  The layout is: a device error
+ * word, per-(row, half) arrival counters, per-unit fp32 partial (m, l) and
+ * per-unit fp32 partial O.  Allocate it once, zero it once (cudaMemset 0),
+ * outside any graph capture; every successful call leaves the counters back
+ * at zero, so it can be reused across calls and batch sizes.  Returns 0 for
+ * arguments out of range.
+ */
+size_t smla_workspace_bytes(int max_rows, int num_heads, int max_splits);
+
+/*
+ * One decode step: validates on the host, then enqueues ONE kernel launch on
+ * `stream` (a grid of num_rows*num_splits CTA pairs, cluster size 2).
+ * Host checks come first: NULL or misaligned pointers, unsupported sizes, a
+ * workspace smaller than smla_workspace_bytes(num_rows, num_heads, num_splits)
+ * and a device that is not sm_103 each return an error and launch nothing.
+ * Device-side lengths and indices may change between CUDA-graph replays; bad
+ * device data sets bits in the workspace error word (SMLA_DEV_*) and never
+ * traps.  Rows with no valid entry get out = 0 and lse = sink (written).
+ * Calls that share a workspace must be ordered on one stream.
+ * Returns SMLA_OK once the launch is enqueued.
+ */
+smla_status smla_decode(const smla_decode_args* args, void* workspace, size_t ws_bytes,
+                        smla_stream_t stream);
+
+/*
+ * Copies the workspace's device error word to *flags (host) and clears it.
+ * Enqueued on `stream` and synchronised with it before returning.
+ */
+smla_status smla_read_device_error(void* workspace, uint32_t* flags, smla_stream_t stream);
+
+/* Static, NUL-terminated description of a status code. */
+const char* smla_status_string(smla_status status);
+
+#ifdef __cplusplus
+}  /* extern "C" */
+#endif
+
+#endif  /* SMLA_H_ */

@@ -1,0 +1,253 @@
+"""CUDA path (through the C ABI) against the float64 oracle, element by element.
+
+Tolerance: |out_gpu - out_ref| <= 1e-2 + 1e-2 |out_ref| (bf16 out) and
+|lse_gpu - lse_ref| <= 1e-3, on the same seeded inputs."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import smla_inputs as I
+import sparse_mla_decode_04_gb300 as smla
+from helpers import assert_close, run_gpu, run_oracle
+
+pytestmark = pytest.mark.gpu
+
+
+def small(H=64, seed=7, seq_lens=(3000, 1500, 700), topk=100, swa=70, invalid=0.1, mild=False, **kw):
+    rows = [(s, L) for s, L in enumerate(seq_lens)]
+    return I.build_problem(name="small", seq_lens=list(seq_lens), rows=rows, H=H, topk=topk, invalid_frac=invalid,
+                           swa=swa, seed=seed, device="cuda", mild=mild, **kw)
+
+
+def check(p, num_splits=None, rows=None, what="", workspace=None):
+    out, lse = run_gpu(p, num_splits=num_splits, workspace=workspace)
+    ro, rl = run_oracle(p, rows=rows)
+    return assert_close(out, lse, ro, rl, rows=rows, what=what or p.name)
+
+
+# ---------------------------------------------------------------------------
+def test_tiny(cuda_device):
+    check(I.tiny(device="cuda"))
+
+
+def test_tiny_mild(cuda_device):
+    check(I.tiny(device="cuda", mild=True))
+
+
+@pytest.mark.parametrize("H", [16, 32, 64, 128, 8, 100])
+@pytest.mark.parametrize("splits", [1, 3])
+@pytest.mark.parametrize("mild", [False, True])
+def test_small_heads_and_splits(cuda_device, H, splits, mild):
+    check(small(H=H, mild=mild), num_splits=splits, what=f"H{H} s{splits} mild{mild}")
+
+
+@pytest.mark.parametrize("splits", [1, 2, 5, 8, 17, 32])
+def test_forced_splits(cuda_device, splits):
+    p = small(H=128, seq_lens=(20000, 12000, 9000, 4000), topk=2048, swa=128, invalid=0.02, seed=11)
+    check(p, num_splits=splits, what=f"splits {splits}")
+
+
+def test_mixed_split_and_unsplit_rows(cuda_device):
+    # one long row takes most of the split budget; the short rows stay unsplit
+    p = small(H=128, seq_lens=(200000, 300, 64, 5000, 1), topk=512, swa=128, invalid=0.05, seed=12)
+    check(p, num_splits=6, what="mixed")
+    check(p, num_splits=1, what="mixed s1")
+
+
+def test_every_row_one_split_on_wide_grid(cuda_device):
+    # grid of rows*splits units where the live lengths give every row one split
+    p = small(H=128, seq_lens=(200, 150, 100, 90), topk=32, swa=16, seed=13)
+    check(p, num_splits=16, what="one split per row on a wide grid")
+
+
+def test_empty_and_degenerate_rows(cuda_device):
+    p = small(H=32, seq_lens=(4000, 4000, 4000, 4000, 4000), topk=256, swa=64, seed=14)
+    p.main_idx[0] = -1          # row 0: no valid top-k, no window, no compressed -> sink only
+    p.swa_len[0] = 0
+    p.cmp_len[0] = 0
+    p.main_idx[1] = -1          # row 1: compressed only (ragged tail)
+    p.swa_len[1] = 0
+    p.cmp_len[1] = 77
+    p.swa_len[2] = 0            # row 2: top-k only
+    p.cmp_len[2] = 0
+    p.main_idx[3] = -1          # row 3: window only
+    p.cmp_len[3] = 0
+    p.cmp_len[4] = 64           # row 4: exactly one full compressed group
+    out, lse = run_gpu(p, num_splits=2)
+    ro, rl = run_oracle(p)
+    assert_close(out, lse, ro, rl, what="degenerate rows")
+    assert torch.count_nonzero(out[0]).item() == 0
+    assert torch.equal(lse[0].cpu(), p.sink.cpu())
+
+
+def test_topk_disabled_and_no_sink(cuda_device):
+    p = small(H=16, seq_lens=(900, 2000), topk=0, swa=100, seed=15, with_sink=False)
+    check(p, num_splits=1, what="no top-k, no sink")
+    check(p, num_splits=4, what="no top-k, no sink, split")
+
+
+def test_duplicate_indices(cuda_device):
+    p = small(H=64, seq_lens=(3000,), topk=128, swa=64, seed=16)
+    p.main_idx[0, 64:] = p.main_idx[0, :64]  # every top-k slot listed twice
+    p.main_idx[0, 5] = int(p.swa_start[0].item()) + 3  # and one also in the window
+    check(p, num_splits=1, what="duplicates")
+
+
+def test_poisoned_unreferenced_memory_is_bit_identical(cuda_device):
+    p = I.build_problem(name="poison", seq_lens=[1024], rows=[(0, 1024), (0, 1024)], H=32, topk=128,
+                        invalid_frac=0.25, swa=64, seed=17, device="cuda", paged=False, pool_entries=1024,
+                        cmp_override=([0, 128], [96, 96], 256), row_seq=True)
+    out_a, lse_a = run_gpu(p, num_splits=2)
+    ref = set()
+    for r in range(2):
+        ref.update(v for v in p.main_idx[r].tolist() if v != -1)
+        s, n = int(p.swa_start[r]), int(p.swa_len[r])
+        ref.update(range(s, s + n))
+    unref = torch.tensor(sorted(set(range(1024)) - ref), device="cuda", dtype=torch.long)
+    assert unref.numel() > 0
+    p.kv_pool[unref] = 0xFF   # NaN e4m3 / NaN bf16 bytes
+    p.kv_scales[unref] = 255  # NaN scale code
+    tail = torch.tensor(list(range(96, 128)) + list(range(224, 256)), device="cuda")
+    p.cmp_pool[tail] = 0xFF
+    p.cmp_scales[tail] = 255
+    out_b, lse_b = run_gpu(p, num_splits=2)
+    assert torch.equal(out_a.view(torch.int16), out_b.view(torch.int16))
+    assert torch.equal(lse_a, lse_b)
+    assert not torch.isnan(out_b.float()).any()
+
+
+def test_determinism_20_launches(cuda_device):
+    p = small(H=128, seq_lens=(30000, 8000), topk=2048, swa=128, seed=18)
+    ws = smla.Workspace(2, 128, 6)
+    out0, lse0 = run_gpu(p, num_splits=6, workspace=ws)
+    for _ in range(19):
+        out, lse = run_gpu(p, num_splits=6, workspace=ws)
+        assert torch.equal(out.view(torch.int16), out0.view(torch.int16))
+        assert torch.equal(lse, lse0)
+    assert ws.read_error() == 0
+
+
+def test_bad_device_data_sets_error_bits_and_is_dropped(cuda_device):
+    p = small(H=16, seq_lens=(2000, 2000, 2000), topk=64, swa=32, seed=19)
+    p.main_idx[0, 3] = -7                 # < -1
+    p.main_idx[0, 4] = 10 ** 6            # beyond the page table
+    p.cmp_start[1] = int(p.cmp_pool.shape[0]) - 10  # compressed range runs off the pool
+    ws = smla.Workspace(3, 16, 2)
+    out, lse = run_gpu(p, num_splits=2, workspace=ws)
+    ro, rl = run_oracle(p)
+    assert_close(out, lse, ro, rl, what="bad data")
+    flags = ws.read_error()
+    assert flags & smla.SMLA_DEV_BAD_INDEX and flags & smla.SMLA_DEV_BAD_CMP
+    assert ws.read_error() == 0  # cleared by the read
+    p.swa_len[2] = -5
+    run_gpu(p, num_splits=2, workspace=ws)
+    assert ws.read_error() & smla.SMLA_DEV_BAD_LENGTH
+
+
+def test_workspace_reuse_across_batch_sizes(cuda_device):
+    ws = smla.Workspace(32, 128, 8)
+    big = small(H=128, seq_lens=tuple([6000] * 12), topk=512, swa=128, seed=20)
+    little = small(H=128, seq_lens=(40000, 100), topk=512, swa=128, seed=21)
+    check(big, num_splits=4, workspace=ws, what="big")
+    check(little, num_splits=8, workspace=ws, what="little")
+    check(big, num_splits=2, workspace=ws, what="big again")
+    assert ws.read_error() == 0
+
+
+def test_graph_replay_with_changing_lengths(cuda_device):
+    p = small(H=128, seq_lens=(2000, 9000, 30000, 60000), topk=1024, swa=128, invalid=0.0, seed=22)
+    R, H = p.num_rows, p.num_heads
+    S = 8
+    ws = smla.Workspace(R, H, S)
+    out = torch.empty((R, H, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((R, H), dtype=torch.float32, device="cuda")
+    smla.decode(p, num_splits=S, out=out, lse=lse, workspace=ws)  # warm-up outside capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            smla.decode(p, num_splits=S, out=out, lse=lse, workspace=ws)
+    for i in range(6):
+        I.redraw_lengths(p, seed=100 + i)
+        g.replay()
+        torch.cuda.synchronize()
+        ro, rl = run_oracle(p)
+        assert_close(out, lse, ro, rl, what=f"replay {i}")
+    assert ws.read_error() == 0
+
+
+def test_int64_addressing_large_pool(cuda_device):
+    # > 2^31 bytes of main pool; indices near its end (identity mapping) and
+    # through a page table whose page ids put rows past 2^31 / 576
+    n = 4_000_000
+    g = torch.Generator(device="cuda")
+    g.manual_seed(23)
+    pool, scales = I.make_pool(n, g, "cuda")
+    assert n * 576 > 2 ** 31
+    R, H, topk = 2, 64, 256
+    q = torch.randn((R, H, 512), generator=g, device="cuda").to(torch.bfloat16)
+    main = torch.randint(n - 50_000, n, (R, topk), generator=g, device="cuda", dtype=torch.int32)
+
+    class P:  # plain attribute bag for smla.decode / the oracle kwargs below
+        pass
+
+    p = P()
+    p.q_nope, p.q_rope = q[:, :, :448].contiguous(), q[:, :, 448:].contiguous()
+    p.kv_pool, p.kv_scales, p.block_table, p.row_seq = pool, scales, None, None
+    p.main_idx, p.topk = main, topk
+    p.swa_start = torch.tensor([n - 100, n - 64], dtype=torch.int32, device="cuda")
+    p.swa_len = torch.tensor([64, 64], dtype=torch.int32, device="cuda")
+    p.cmp_pool, p.cmp_scales, p.cmp_start, p.cmp_len = None, None, None, None
+    p.sink = torch.randn((H,), generator=g, device="cuda")
+    p.sm_scale = 512 ** -0.5
+    out, lse = run_gpu(p, num_splits=2)
+    kw = dict(q_nope=p.q_nope.view(torch.int16).cpu().numpy().view(np.uint16),
+              q_rope=p.q_rope.view(torch.int16).cpu().numpy().view(np.uint16),
+              kv_pool=I.RowReader(pool), kv_scales=I.RowReader(scales), main_idx=main.cpu().numpy(),
+              swa_start=p.swa_start.cpu().numpy(), swa_len=p.swa_len.cpu().numpy(), cmp_pool=None,
+              cmp_scales=None, cmp_start=None, cmp_len=None, sink=p.sink.cpu().numpy(), sm_scale=p.sm_scale)
+    ro, rl = oracle.decode(**kw)
+    assert_close(out, lse, ro, rl, what="int64 identity")
+    # paged: 2 sequences whose pages sit at the top of the pool
+    pages = n // 64
+    p.block_table = torch.tensor([[pages - 1, pages - 3], [pages - 2, 5]], dtype=torch.int32, device="cuda")
+    p.main_idx = torch.randint(0, 128, (R, topk), generator=g, device="cuda", dtype=torch.int32)
+    p.swa_start = torch.tensor([60, 100], dtype=torch.int32, device="cuda")
+    p.swa_len = torch.tensor([64, 28], dtype=torch.int32, device="cuda")
+    out, lse = run_gpu(p, num_splits=1)
+    kw.update(main_idx=p.main_idx.cpu().numpy(), swa_start=p.swa_start.cpu().numpy(),
+              swa_len=p.swa_len.cpu().numpy(), block_table=p.block_table.cpu().numpy())
+    ro, rl = oracle.decode(**kw)
+    assert_close(out, lse, ro, rl, what="int64 paged")
+
+
+# ---------------------------------------------------------------------------
+# full-size workloads, sampled rows (the oracle computes them one by one)
+# ---------------------------------------------------------------------------
+def test_dsv4_decode_sampled_rows(cuda_device):
+    p = I.dsv4(device="cuda")
+    S = smla.smla_plan_num_splits(p.num_rows, p.num_heads, p.kv_len_estimate())
+    out, lse = run_gpu(p, num_splits=S)
+    rows = [0, 13, 31]
+    ro, rl = run_oracle(p, rows=rows)
+    assert_close(out, lse, ro, rl, rows=rows, what="dsv4")
+    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+
+
+def test_mtp_decode_sampled_rows(cuda_device):
+    p = I.mtp(device="cuda")
+    S = smla.smla_plan_num_splits(p.num_rows, p.num_heads, p.kv_len_estimate())
+    out, lse = run_gpu(p, num_splits=S)
+    rows = [0, 1, 2, 3, 37, 63]
+    ro, rl = run_oracle(p, rows=rows)
+    assert_close(out, lse, ro, rl, rows=rows, what="mtp")
+
+
+def test_ragged_long_context_all_rows(cuda_device):
+    p = I.ragged(device="cuda")
+    S = smla.smla_plan_num_splits(p.num_rows, p.num_heads, p.kv_len_estimate())
+    out, lse = run_gpu(p, num_splits=S)
+    ro, rl = run_oracle(p)
+    assert_close(out, lse, ro, rl, what="ragged")
