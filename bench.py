@@ -293,6 +293,7 @@ def run_gpu(args):
     events = []
     with ClockSampler(local) as clocks:
         t_wall = time.perf_counter()
+        torch.cuda.nvtx.range_push("timed")
         with torch.cuda.stream(stream):
             for _ in range(args.steps):
                 flush_buf.fill_(2)
@@ -303,6 +304,7 @@ def run_gpu(args):
                 e1.record(stream)
                 events.append((e0, e1))
         barrier()
+        torch.cuda.nvtx.range_pop()
         t_wall = time.perf_counter() - t_wall
     kernel_ms = [a.elapsed_time(b) for a, b in events]
     ms_step = reduce_max(statistics.mean(kernel_ms))

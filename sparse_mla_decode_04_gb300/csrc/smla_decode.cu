@@ -539,6 +539,7 @@ smla_decode_kernel(const KParams p) {
                 oscale = Z > 0.f ? wm / Z : 0.f;
                 lse = (M + log2f(Z)) * kLn2;
             }
+            if (lsum == 0.f) lse = (a.sink != nullptr && h < H) ? __ldg(a.sink + h) : -INFINITY;  // sink only, exactly
             uint16_t* outp = static_cast<uint16_t*>(a.out) + ((size_t)r * H + (h < H ? h : 0)) * SMLA_HEAD_DIM + 256 * crank;
 #pragma unroll 1
             for (int c = 0; c < 8; ++c) {
@@ -594,12 +595,13 @@ smla_decode_kernel(const KParams p) {
                 if (h < H) {
                     float M = sink2;
                     for (int i = 0; i < s_r; ++i) M = fmaxf(M, __ldcg(p.ml + ((size_t)(row_u0 + i) * 2 + crank) * H + h).x);
-                    float Z = 0.f;
+                    float Z = 0.f, lall = 0.f;
                     if (M != -INFINITY) {
                         Z = (sink2 == -INFINITY) ? 0.f : exp2f(sink2 - M);
                         for (int i = 0; i < s_r; ++i) {
                             const float2 ml = __ldcg(p.ml + ((size_t)(row_u0 + i) * 2 + crank) * H + h);
                             if (ml.x != -INFINITY) Z += ml.y * exp2f(ml.x - M);
+                            lall += ml.y;
                         }
                     }
                     const float inv = Z > 0.f ? 1.f / Z : 0.f;
@@ -634,8 +636,11 @@ smla_decode_kernel(const KParams p) {
                             *reinterpret_cast<uint4*>(outp + 32 * c + 8 * q) = wv;
                         }
                     }
-                    if (crank == 0 && a.lse != nullptr)
-                        a.lse[(size_t)r * H + h] = (M == -INFINITY || Z <= 0.f) ? -INFINITY : (M + log2f(Z)) * kLn2;
+                    if (crank == 0 && a.lse != nullptr) {
+                        float lse = (M == -INFINITY || Z <= 0.f) ? -INFINITY : (M + log2f(Z)) * kLn2;
+                        if (lall == 0.f) lse = a.sink != nullptr ? __ldg(a.sink + h) : -INFINITY;  // sink only, exactly
+                        a.lse[(size_t)r * H + h] = lse;
+                    }
                 }
                 if (tid == 0) atomicExch(p.counters + 2 * r + crank, 0u);
             }
