@@ -177,6 +177,38 @@ smla_status smla_read_device_error(void* workspace, uint32_t* flags, smla_stream
 /* Static, NUL-terminated description of a status code. */
 const char* smla_status_string(smla_status status);
 
+/* Bytes of the scratch array built into the library for smla_decode_static_scratch. */
+#define SMLA_STATIC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+/*
+ * smla_decode for callers that cannot allocate device memory.  The pages have
+ * no counterpart to this entry point.
+ *
+ * Some callers have no way to call cudaMalloc: plugin or custom-op interfaces
+ * that hand a kernel only its inputs, outputs and a stream; code that runs
+ * while a CUDA graph is being captured (cudaMalloc is not a stream operation);
+ * processes whose device memory is owned entirely by another allocator.  This
+ * entry point allocates nothing: its scratch (the same layout as the
+ * smla_decode workspace) is a file-scope __device__ array of
+ * SMLA_STATIC_SCRATCH_BYTES (32 MiB) that every GPU which loads the library
+ * holds until the process exits.  The caller still passes every input and
+ * output in `args`.
+ *
+ * - Calls whose smla_workspace_bytes(num_rows, num_heads, num_splits) exceeds
+ *   SMLA_STATIC_SCRATCH_BYTES return SMLA_ERR_WORKSPACE_TOO_SMALL and launch
+ *   nothing; shrink num_splits or the batch.
+ * - The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current) and caches it; make that
+ *   first call before any stream capture on the device.
+ * - Every call on a device shares the one array, and the array keeps what the
+ *   last call left.  Each call clears the error word and arrival counters on
+ *   `stream` before its launch, so the SMLA_DEV_* flags of a call cannot be
+ *   read back through this entry point.  Calls that overlap on the GPU (other
+ *   streams, other host threads) race on the array: order them on one stream.
+ * - Otherwise it behaves as smla_decode, including its host checks.
+ */
+smla_status smla_decode_static_scratch(const smla_decode_args* args, smla_stream_t stream);
+
 #ifdef __cplusplus
 }  /* extern "C" */
 #endif

@@ -22,7 +22,7 @@ LIB_DIR = PKG / "lib"
 LIB_NAME = "libsmla.so"
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
-SOURCES = ["smla_decode.cu", "smla_host.cpp"]
+SOURCES = ["smla_decode.cu", "smla_host.cpp", "smla_static_scratch.cu"]
 
 
 def nvcc_path() -> str:

@@ -161,3 +161,14 @@ def make_args(*, q_nope, q_rope, kv_pool, kv_scales, main_idx, topk, swa_start, 
     a.num_rows, a.num_heads = int(q_nope.shape[0]), int(q_nope.shape[1])
     a.num_splits = int(num_splits)
     return a
+
+
+def smla_decode_static_scratch(args: smla_decode_args, stream: int = 0) -> int:
+    """smla_decode with the library's built-in scratch array instead of a
+    caller-allocated workspace (for callers that cannot allocate device
+    memory; see include/smla.h).  Returns the status."""
+    lib = load_library()
+    fn = lib.smla_decode_static_scratch
+    fn.argtypes = [POINTER(smla_decode_args), c_void_p]
+    fn.restype = c_int
+    return fn(ctypes.byref(args), c_void_p(stream))
