@@ -9,38 +9,40 @@
 // nm] Split plan helper and persistent decode kernel with in-kernel split and
 // merge", summary part 2.
 //
-// GB300 design.  A work unit is (row, split) and runs on a CTA pair (cluster
-// of 2); CTA c owns dims [256c, 256c+256) of the 512-wide head dim, because O
-// for 128 heads x 512 dims in fp32 would fill a whole SM's TMEM.  The grid is
-// persistent: each cluster walks its share of the units.  Inside a CTA the
-// work is split over warp roles that hand 64-entry tiles along mbarrier rings:
+// GB300 design.  A work unit is (row, split).  O for 128 heads x 512 dims in
+// fp32 would fill a whole SM's TMEM, so each unit runs on two CTAs and CTA c
+// owns output dims [256c, 256c+256).  The two CTAs share nothing: each one
+// gathers the whole entries and computes the full 512-wide QK itself, so both
+// hold bit-identical scores and make identical softmax decisions, and no data
+// crosses SMs (moving partial scores between SMs through distributed shared
+// memory measured ~2.5 us per 32 KB, several times the tensor time of a tile).
+// The grid is persistent.  Inside a CTA, warp roles pass 32-entry tiles along
+// mbarrier rings:
 //
-//   producer warps (4)   resolve a tile's slots (top-k index -> page table ->
-//                        64-bit row; window; compressed) and issue one bulk
-//                        copy per valid entry of this CTA's half of its bytes
-//                        into a 4-stage raw ring, plus the entry's scale codes;
-//   dequant warps (4)    raw ring -> bf16 tile (e4m3 x 2^(code-127), exact) in
-//                        a 3-stage ring of 128-byte-swizzled tiles, each of
-//                        which is the K-major B operand of QK and the MN-major
-//                        B operand of PV;
-//   MMA warp (1 thread)  QK(t) = Q . X(t)^T on tcgen05 (M = 128 heads, N = 64,
-//                        K = 256, A = Q from TMEM), then PV(t-1);
-//   softmax warps (4)    one thread per head (TMEM lane): partial scores are
-//                        swapped with the peer CTA through distributed shared
-//                        memory and summed (fp32 addition commutes, so both CTAs
-//                        hold identical scores), online softmax with a
-//                        conditional rescale, and P written back into the score
-//                        columns of TMEM as a bf16 pair hi = bf16(p),
-//                        lo = bf16(p - hi) for PV (A from TMEM).  A single bf16
-//                        P (8-bit mantissa) is not enough: with V near 600 in
-//                        magnitude, nearly tied entries whose V values cancel
+//   producer warps (3)   one per raw stage: resolve a tile's 32 slots (top-k index -> page table
+//                        -> 64-bit row; window; compressed) and issue one bulk
+//                        copy per valid entry (576 B) plus a cp.async of its 8
+//                        scale bytes into a 3-stage raw ring;
+//   dequant warps (4)    raw ring -> bf16 (e4m3 x 2^(code-127), exact) in a
+//                        3-stage ring of 128-byte-swizzled [8 atoms][32][128 B]
+//                        tiles: the K-major B operand of QK and, through the
+//                        atoms of this CTA's dims, the MN-major B of PV;
+//   MMA warp (1 thread)  QK(t): M = 128 heads, N = 32, K = 512 with Q dims
+//                        0..255 from TMEM and 256..511 from shared memory;
+//                        then PV(t-1): M = 128, N = 256, K = 32 with P from TMEM;
+//   softmax warps (4)    one thread per head (TMEM lane): online softmax with a
+//                        conditional rescale, P written back over the scores as
+//                        a bf16 pair hi = bf16(p), lo = bf16(p - hi).  A single
+//                        bf16 P (8-bit mantissa) is not enough: with V near 600
+//                        in magnitude, nearly tied entries whose V values cancel
 //                        would carry errors near 1.  The lo half is skipped on
 //                        tiles where a running bound (sum |lo| x max |V|) shows
 //                        its total effect on every head's output stays within
 //                        2^-9; on peaked softmaxes most tiles qualify.
 //
-// TMEM (512 columns): O [0, 256), two score/P buffers [256, 384), Q [384, 512).
-// Heads beyond num_heads are zero-padded up to the MMA's M = 128.
+// TMEM (512 columns): O [0, 256), two score/P buffers [256, 320), Q dims
+// 0..255 as bf16 pairs [320, 448).  Heads beyond num_heads are zero-padded up
+// to the MMA's M = 128.
 #include <algorithm>
 #include <cstdint>
 #include <cstring>
@@ -56,24 +58,26 @@
 
 namespace smla {
 
-constexpr int kBK = 64;               // entries per tile
-constexpr int kNR = 4;                // raw-byte ring stages
+constexpr int kBK = 32;               // entries per tile
+constexpr int kNR = 3;                // raw-byte ring stages
 constexpr int kNX = 3;                // bf16 tile ring stages
 constexpr int kSoftmaxWarps = 4;      // warps 0-3: one thread per head
-constexpr int kProducerWarp0 = 4;     // warps 4-7: one producer per raw stage
-constexpr int kNumProducers = kNR;
-constexpr int kMmaWarp = 8;
-constexpr int kDequantWarp0 = 9;      // warps 9-12
+constexpr int kProducerWarp0 = 4;     // warps 4-6: producer pw owns raw stage pw (tiles g % kNR == pw)
+constexpr int kNumProducers = kNR;    // one per stage: each waits its stage's phases strictly in order
+constexpr int kMmaWarp = 7;
+constexpr int kDequantWarp0 = 8;      // warps 8-11
 constexpr int kNumDequantWarps = 4;
-constexpr int kWarps = 13;
+constexpr int kWarps = 12;
 constexpr int kThreads = 32 * kWarps;
-constexpr int kHeadsPad = 128;
-constexpr int kMaxUnitsPerCluster = 32;
+constexpr int kHeadsPad = 128;        // heads padded up to the MMA M
+static_assert(kHeadsPad == 32 * kSoftmaxWarps, "one softmax thread per padded head");
+static_assert(kBK == 32, "one producer lane per slot");
+constexpr int kMaxUnitsPerPair = 32;
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;        // O half: columns [0, 256)
-constexpr uint32_t kTmemS = 256;      // score / P buffers: [256, 320), [320, 384)
-constexpr uint32_t kTmemQ = 384;      // Q half, bf16 packed: [384, 512)
+constexpr uint32_t kTmemS = 256;      // score / P buffers: [256, 288), [288, 320)
+constexpr uint32_t kTmemQ = 320;      // Q dims 0..255, bf16 packed: [320, 448)
 constexpr uint64_t kWaitNs = 2000000000ull;  // bounded-wait limit (2 s)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -83,34 +87,34 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: P may grow to 2^8 befo
 // denominator: the output error from skipping is then at most kLoBudget.
 constexpr float kLoBudget = 1.0f / 512.0f;
 
-constexpr uint32_t kRawEntryBytes = 320;   // CTA0 uses 256 of them, CTA1 all 320
-constexpr uint32_t kXStageBytes = 4 * kBK * 128;           // 32 KB
-constexpr uint32_t kRawStageBytes = kBK * kRawEntryBytes;  // 20 KB
+constexpr uint32_t kAtomBytes = kBK * 128;                   // one 64-dim atom of a tile: 4 KB
+constexpr uint32_t kXStageBytes = 8 * kAtomBytes;            // 32 KB
+constexpr uint32_t kRawStageBytes = kBK * SMLA_ENTRY_BYTES;  // 18 KB
 
 // Shared-memory layout (offsets from a 1024-byte-aligned base).
-constexpr uint32_t kOffX = 0;                                   // [kNX][4 atoms][64][128 B]
-constexpr uint32_t kOffRaw = kOffX + kNX * kXStageBytes;        // [kNR][64][320 B]
-constexpr uint32_t kOffRawSc = kOffRaw + kNR * kRawStageBytes;  // [kNR][64] u64 scale codes
-constexpr uint32_t kOffSin = kOffRawSc + kNR * kBK * 8;         // peer's partial S [128][64] f32 (32 KB)
-constexpr uint32_t kOffRawMask = kOffSin + 32768;               // [kNR] u64 valid masks
-constexpr uint32_t kOffXMask = kOffRawMask + kNR * 8;           // [kNX] u64 valid masks
-constexpr uint32_t kOffXVmax = kOffXMask + 32;                  // [kNX][4 dequant warps] f32 max |V| bound
+constexpr uint32_t kOffQ = 0;                                   // Q dims 256..511: [4 atoms][128][128 B]
+constexpr uint32_t kOffX = kOffQ + 65536;                       // [kNX][8 atoms][32][128 B]
+constexpr uint32_t kOffRaw = kOffX + kNX * kXStageBytes;        // [kNR][32][576 B]
+constexpr uint32_t kOffRawSc = kOffRaw + kNR * kRawStageBytes;  // [kNR][32] u64 scale codes
+constexpr uint32_t kOffRawMask = kOffRawSc + kNR * kBK * 8;     // [kNR] u32 valid masks
+constexpr uint32_t kOffXMask = kOffRawMask + 16;                // [kNX] u32 valid masks
+constexpr uint32_t kOffXVmax = kOffXMask + 16;                  // [kNX][4 dequant warps] f32 max |V| bound
 constexpr uint32_t kOffVote = kOffXVmax + kNX * 16;             // [2][4 softmax warps] u32 lo-skip votes
 constexpr uint32_t kOffBar = kOffVote + 32;                     // mbarriers
 constexpr uint32_t kNumBars = 32;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;           // tmem base, flags, reductions
 constexpr uint32_t kMiscBytes = 512;
 constexpr uint32_t kOffUnits = kOffMisc + kMiscBytes;           // unit descriptors
-constexpr uint32_t kSmemUsed = kOffUnits + kMaxUnitsPerCluster * 32;
+constexpr uint32_t kSmemUsed = kOffUnits + kMaxUnitsPerPair * 32;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;               // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-// The plan's per-row scratch (tiles[R], prefix[R+1]) aliases the exchange buffer
-// during the prologue; a cluster barrier separates it from the first exchange.
-static_assert(4 * (2 * SMLA_MAX_ROWS + 8) <= 32768, "plan scratch fits in the exchange buffer");
+// The plan's per-row scratch (tiles[R], prefix[R+1]) aliases the raw ring
+// during the prologue, before any producer runs.
+static_assert(4 * (2 * SMLA_MAX_ROWS + 8) <= kNR * kRawStageBytes, "plan scratch fits in the raw ring");
 
 // mbarrier indices
 enum : uint32_t {
-    BAR_RAW_FULL = 0,                      // [kNR] producer -> dequant (1 arrival + tx bytes)
+    BAR_RAW_FULL = 0,                      // [kNR] producer -> dequant (32 async + 1 arrival, tx bytes)
     BAR_RAW_EMPTY = BAR_RAW_FULL + kNR,    // [kNR] dequant -> producer (kNumDequantWarps)
     BAR_X_FULL = BAR_RAW_EMPTY + kNR,      // [kNX] dequant -> MMA, softmax (kNumDequantWarps)
     BAR_X_EMPTY = BAR_X_FULL + kNX,        // [kNX] MMA commit after PV
@@ -118,9 +122,7 @@ enum : uint32_t {
     BAR_P_FULL = BAR_S_FULL + 2,           // [2] softmax -> MMA (kSoftmaxWarps)
     BAR_O_DONE = BAR_P_FULL + 2,           // MMA commit after each PV
     BAR_Q_READY = BAR_O_DONE + 1,          // softmax -> MMA, once per unit (kSoftmaxWarps)
-    BAR_EX_FULL = BAR_Q_READY + 1,         // peer's partial S landed (kHeadsPad remote arrivals)
-    BAR_EX_EMPTY = BAR_EX_FULL + 1,        // peer consumed our partial S (kHeadsPad remote arrivals)
-    BAR_MMA_FINAL = BAR_EX_EMPTY + 1,      // teardown: all MMAs retired
+    BAR_MMA_FINAL = BAR_Q_READY + 1,       // teardown: all MMAs retired
     BAR_COUNT = BAR_MMA_FINAL + 1
 };
 static_assert(BAR_COUNT <= kNumBars, "barrier slots");
@@ -241,20 +243,19 @@ __device__ __forceinline__ int row_tiles(const smla_decode_args& a, int r, uint3
 struct Ctx {
     uint32_t sb;              // shared base (1024-aligned)
     uint32_t tmem;            // TMEM base address
-    uint32_t crank, peer;
+    uint32_t half;            // 0 or 1: output dims [256 half, 256 half + 256)
     volatile uint32_t* abort; // set by any role whose bounded wait gave up
 };
 
 __device__ __forceinline__ uint32_t bar_addr(const Ctx& c, uint32_t i) { return c.sb + kOffBar + 8 * i; }
 
 // Bounded wait that also gives up as soon as another role of this CTA aborted.
-template <bool kCluster>
 __device__ __forceinline__ bool wait_bar(const Ctx& c, uint32_t bar, uint32_t parity) {
-    if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (;;) {
-        for (int i = 0; i < 32; ++i)
-            if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+        for (int i = 0; i < 4; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
         if (*c.abort) return false;
         if (global_timer_ns() - t0 > kWaitNs) {
             *c.abort = 1u;
@@ -265,18 +266,25 @@ __device__ __forceinline__ bool wait_bar(const Ctx& c, uint32_t bar, uint32_t pa
 
 // The same wait, taken by a whole warp: the outcome is made warp-uniform so
 // that the warp never splits around warp-synchronous code after a timeout.
-template <bool kCluster>
 __device__ __forceinline__ bool wait_bar_warp(const Ctx& c, uint32_t bar, uint32_t parity) {
-    const bool ok = wait_bar<kCluster>(c, bar, parity);
+    const bool ok = wait_bar(c, bar, parity);
     return __all_sync(0xffffffffu, ok);
 }
 
-__device__ __forceinline__ void st_shared_u64(uint32_t addr, uint64_t v) {
-    asm volatile("st.shared.b64 [%0], %1;" :: "r"(addr), "l"(v) : "memory");
+__device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared.u32 [%0], %1;" :: "r"(addr), "r"(v) : "memory");
 }
-__device__ __forceinline__ uint64_t ld_shared_u64(uint32_t addr) {
-    uint64_t v;
-    asm volatile("ld.shared.b64 %0, [%1];" : "=l"(v) : "r"(addr) : "memory");
+__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_shared_f32(uint32_t addr, float v) {
+    asm volatile("st.shared.f32 [%0], %1;" :: "r"(addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
     return v;
 }
 __device__ __forceinline__ uint32_t ld_shared_u8(uint32_t addr) {
@@ -303,14 +311,14 @@ __device__ __forceinline__ bool softmax_all(bool v) {
 }
 
 // ---------------------------------------------------------------------------
-// role: producer (one warp per raw stage; warp pw handles tiles g % kNR == pw)
+// role: producer (warp pw owns raw stage pw: tiles g % kNR == pw; lane = slot).
+// A parity wait cannot tell "two phases ahead" from "previous phase done", so
+// each stage has exactly one producer, which waits its phases in order.
 // ---------------------------------------------------------------------------
 __device__ void producer_role(const KParams& p, const Ctx& c, const UnitDesc* units, int n_units, int pw,
                               uint32_t& err) {
     const smla_decode_args& a = p.a;
     const int lane = threadIdx.x & 31;
-    const uint32_t off = c.crank == 0 ? 0u : 256u;
-    const uint32_t bytes = c.crank == 0 ? 256u : 320u;
     uint32_t g = 0;
     for (int ui = 0; ui < n_units; ++ui) {
         const UnitDesc d = units[ui];
@@ -325,65 +333,55 @@ __device__ void producer_role(const KParams& p, const Ctx& c, const UnitDesc* un
         for (int t = d.t_begin; t < d.t_end; ++t, ++g) {
             if ((int)(g % kNR) != pw) continue;
             const uint32_t rs = g % kNR, rph = (g / kNR) & 1u;
-            // resolve this lane's two slots
-            const uint8_t* ep[2] = {nullptr, nullptr};
-            const uint8_t* sp[2] = {nullptr, nullptr};
-#pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                const int slot = lane + 32 * k;
-                long long phys = -1;
-                bool cmp = false;
-                if (t < nmt) {
-                    const int j = t * kBK + slot;
-                    if (j < a.topk) {
-                        const int idx = __ldg(a.main_idx + (size_t)r * a.topk + j);
-                        if (idx != -1) {
-                            phys = map_position(a, idx, seq);
-                            if (phys < 0) err |= SMLA_DEV_BAD_INDEX;
-                        }
-                    }
-                } else if (t < nmt + nst) {
-                    const int j = (t - nmt) * kBK + slot;
-                    if (j < swa_len) {
-                        phys = map_position(a, (long long)swa_start + j, seq);
+            // resolve this lane's slot
+            long long phys = -1;
+            bool cmp = false;
+            if (t < nmt) {
+                const int j = t * kBK + lane;
+                if (j < a.topk) {
+                    const int idx = __ldg(a.main_idx + (size_t)r * a.topk + j);
+                    if (idx != -1) {
+                        phys = map_position(a, idx, seq);
                         if (phys < 0) err |= SMLA_DEV_BAD_INDEX;
                     }
-                } else {
-                    const int j = (t - nmt - nst) * kBK + slot;
-                    if (j < cmp_len) {
-                        cmp = true;
-                        phys = cmp_start + j;
-                        if (phys < 0 || phys >= a.n_cmp) {
-                            err |= SMLA_DEV_BAD_CMP;
-                            phys = -1;
-                        }
+                }
+            } else if (t < nmt + nst) {
+                const int j = (t - nmt) * kBK + lane;
+                if (j < swa_len) {
+                    phys = map_position(a, (long long)swa_start + j, seq);
+                    if (phys < 0) err |= SMLA_DEV_BAD_INDEX;
+                }
+            } else {
+                const int j = (t - nmt - nst) * kBK + lane;
+                if (j < cmp_len) {
+                    cmp = true;
+                    phys = cmp_start + j;
+                    if (phys < 0 || phys >= a.n_cmp) {
+                        err |= SMLA_DEV_BAD_CMP;
+                        phys = -1;
                     }
                 }
-                if (phys >= 0) {
-                    ep[k] = static_cast<const uint8_t*>(cmp ? a.cmp_pool : a.kv_pool) + phys * SMLA_ENTRY_BYTES;
-                    sp[k] = static_cast<const uint8_t*>(cmp ? a.cmp_scales : a.kv_scales) + phys * SMLA_SCALE_BYTES;
-                }
             }
-            const uint32_t m0 = __ballot_sync(0xffffffffu, ep[0] != nullptr);
-            const uint32_t m1 = __ballot_sync(0xffffffffu, ep[1] != nullptr);
-            if (!wait_bar_warp<false>(c, bar_addr(c, BAR_RAW_EMPTY + rs), rph ^ 1u)) return;
+            const uint8_t* ep = nullptr;
+            const uint8_t* sp = nullptr;
+            if (phys >= 0) {
+                ep = static_cast<const uint8_t*>(cmp ? a.cmp_pool : a.kv_pool) + phys * SMLA_ENTRY_BYTES;
+                sp = static_cast<const uint8_t*>(cmp ? a.cmp_scales : a.kv_scales) + phys * SMLA_SCALE_BYTES;
+            }
+            const uint32_t mask = __ballot_sync(0xffffffffu, ep != nullptr);
+            if (!wait_bar_warp(c, bar_addr(c, BAR_RAW_EMPTY + rs), rph ^ 1u)) return;
             const uint32_t full = bar_addr(c, BAR_RAW_FULL + rs);
-            if (lane == 0) mbar_expect_tx_only(full, (uint32_t)(__popc(m0) + __popc(m1)) * bytes);
+            if (lane == 0) mbar_expect_tx_only(full, (uint32_t)__popc(mask) * SMLA_ENTRY_BYTES);
             __syncwarp();
-            const uint32_t raw = c.sb + kOffRaw + rs * kRawStageBytes;
-#pragma unroll
-            for (int k = 0; k < 2; ++k)
-                if (ep[k] != nullptr) bulk_g2s(raw + (lane + 32 * k) * kRawEntryBytes, ep[k] + off, bytes, full);
-#pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                uint2 sc = make_uint2(0u, 0u);
-                if (sp[k] != nullptr) sc = ld_global_nc_v2(sp[k]);
-                st_shared_u64(c.sb + kOffRawSc + (rs * kBK + lane + 32 * k) * 8,
-                              (uint64_t)sc.x | ((uint64_t)sc.y << 32));
+            if (ep != nullptr) {
+                bulk_g2s(c.sb + kOffRaw + rs * kRawStageBytes + lane * SMLA_ENTRY_BYTES, ep, SMLA_ENTRY_BYTES, full);
+                cp_async_8(c.sb + kOffRawSc + (rs * kBK + lane) * 8, sp);
             }
-            if (lane == 0) st_shared_u64(c.sb + kOffRawMask + rs * 8, (uint64_t)m0 | ((uint64_t)m1 << 32));
-            __syncwarp();
-            if (lane == 0) mbar_arrive_local(full);
+            cp_async_arrive_noinc(full);  // one of the 32 async arrivals
+            if (lane == 0) {
+                st_shared_u32(c.sb + kOffRawMask + rs * 4, mask);
+                mbar_arrive_local(full);  // the 33rd arrival, ordered after the mask store
+            }
         }
     }
 }
@@ -391,52 +389,81 @@ __device__ void producer_role(const KParams& p, const Ctx& c, const UnitDesc* un
 // ---------------------------------------------------------------------------
 // role: dequant (4 warps): raw ring -> bf16 swizzled tile ring
 // ---------------------------------------------------------------------------
+// Work items: 32 entries x 28 fp8 chunks (16 dims each, atom k/4, UE8M0 group
+// k/4) and 32 entries x 8 bf16 RoPE chunks (atom 7), spread over 128 threads.
+// Every thread loads all of its chunks first, then converts and stores them.
+// It also returns a bound on |x| over the values of this CTA's dims half.
+__device__ __forceinline__ float dequant_tile(uint32_t raw, uint32_t rawsc, uint32_t xb, uint32_t mask, int dtid,
+                                              uint32_t half) {
+    constexpr int kThreadsD = kNumDequantWarps * 32;
+    constexpr int kItems = kBK * 28 / kThreadsD;  // 7
+    constexpr int kRItems = kBK * 8 / kThreadsD;  // 2
+    float vbound = 0.f;
+    uint4 v[kItems];
+    uint32_t code[kItems];
+#pragma unroll
+    for (int it = 0; it < kItems; ++it) {
+        const int idx = dtid + it * kThreadsD;
+        const int e = idx / 28, k = idx % 28;
+        v[it] = make_uint4(0u, 0u, 0u, 0u);
+        code[it] = 127u;
+        if ((mask >> e) & 1u) {
+            v[it] = ld_shared_v4(raw + e * SMLA_ENTRY_BYTES + 16 * k);
+            code[it] = ld_shared_u8(rawsc + e * 8 + (k >> 2));
+        }
+    }
+    uint4 rv[kRItems];
+#pragma unroll
+    for (int it = 0; it < kRItems; ++it) {
+        const int idx = dtid + it * kThreadsD;
+        const int e = idx >> 3, k = idx & 7;
+        rv[it] = make_uint4(0u, 0u, 0u, 0u);
+        if ((mask >> e) & 1u) rv[it] = ld_shared_v4(raw + e * SMLA_ENTRY_BYTES + SMLA_NOPE_DIMS + 16 * k);
+    }
+#pragma unroll
+    for (int it = 0; it < kItems; ++it) {
+        const int idx = dtid + it * kThreadsD;
+        const int e = idx / 28, k = idx % 28;
+        const float scale = ue8m0_to_f32(code[it]);
+        uint32_t o[8];
+        dequant16(v[it], scale, o);
+        if ((uint32_t)(k >> 4) == half) {  // dims 16k.. lie in this CTA's half
+            const float bnd = e4m3x16_absmax(v[it]) * scale;
+            vbound = (bnd > vbound || bnd != bnd) ? (bnd != bnd ? INFINITY : bnd) : vbound;
+        }
+        const uint32_t dst = xb + (k >> 2) * kAtomBytes;
+        const int kk = (k & 3) * 2;
+        st_shared_v4(dst + sw128_offset(e, kk), o[0], o[1], o[2], o[3]);
+        st_shared_v4(dst + sw128_offset(e, kk + 1), o[4], o[5], o[6], o[7]);
+    }
+#pragma unroll
+    for (int it = 0; it < kRItems; ++it) {
+        const int idx = dtid + it * kThreadsD;
+        const int e = idx >> 3, k = idx & 7;
+        if (half == 1u) vbound = fmaxf(vbound, bf16x8_absmax(rv[it]));
+        st_shared_v4(xb + 7 * kAtomBytes + sw128_offset(e, k), rv[it].x, rv[it].y, rv[it].z, rv[it].w);
+    }
+    return vbound;
+}
+
 __device__ void dequant_role(const Ctx& c, const UnitDesc* units, int n_units, int dw) {
     const int lane = threadIdx.x & 31;
     const int dtid = dw * 32 + lane;
-    const int nch = c.crank == 0 ? 16 : 20;
     uint32_t g = 0;
     for (int ui = 0; ui < n_units; ++ui) {
         const int n = units[ui].t_end - units[ui].t_begin;
         for (int i = 0; i < n; ++i, ++g) {
             const uint32_t rs = g % kNR, rph = (g / kNR) & 1u;
             const uint32_t xs = g % kNX, xph = (g / kNX) & 1u;
-            if (!wait_bar_warp<false>(c, bar_addr(c, BAR_RAW_FULL + rs), rph)) return;
-            if (!wait_bar_warp<false>(c, bar_addr(c, BAR_X_EMPTY + xs), xph ^ 1u)) return;
-            const uint64_t mask = ld_shared_u64(c.sb + kOffRawMask + rs * 8);
-            const uint32_t raw = c.sb + kOffRaw + rs * kRawStageBytes;
-            const uint32_t xb = c.sb + kOffX + xs * kXStageBytes;
-            float vbound = 0.f;  // >= |x| for every value this thread wrote
-            for (int idx = dtid; idx < kBK * nch; idx += kNumDequantWarps * 32) {
-                const int e = idx / nch, k = idx - e * nch;
-                const bool valid = ((mask >> e) & 1ull) != 0ull;
-                if (c.crank == 0 || k < 12) {
-                    const int atom = k >> 2, kk = (k & 3) * 2;
-                    uint32_t o[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-                    if (valid) {
-                        const uint4 v = ld_shared_v4(raw + e * kRawEntryBytes + 16 * k);
-                        const uint32_t byte0 = (c.crank == 0 ? 0u : 256u) + 16u * (uint32_t)k;
-                        const uint32_t code = ld_shared_u8(c.sb + kOffRawSc + (rs * kBK + e) * 8 + (byte0 >> 6));
-                        const float scale = ue8m0_to_f32(code);
-                        dequant16(v, scale, o);
-                        const float bnd = e4m3x16_absmax(v) * scale;
-                        vbound = (bnd > vbound || bnd != bnd) ? (bnd != bnd ? INFINITY : bnd) : vbound;
-                    }
-                    const uint32_t dst = xb + atom * (kBK * 128);
-                    st_shared_v4(dst + sw128_offset(e, kk), o[0], o[1], o[2], o[3]);
-                    st_shared_v4(dst + sw128_offset(e, kk + 1), o[4], o[5], o[6], o[7]);
-                } else {
-                    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-                    if (valid) v = ld_shared_v4(raw + e * kRawEntryBytes + 16 * k);
-                    vbound = fmaxf(vbound, bf16x8_absmax(v));
-                    st_shared_v4(xb + 3 * (kBK * 128) + sw128_offset(e, k - 12), v.x, v.y, v.z, v.w);
-                }
-            }
-            if (dtid == 0) st_shared_u64(c.sb + kOffXMask + xs * 8, mask);
+            if (!wait_bar_warp(c, bar_addr(c, BAR_RAW_FULL + rs), rph)) return;
+            if (!wait_bar_warp(c, bar_addr(c, BAR_X_EMPTY + xs), xph ^ 1u)) return;
+            const uint32_t mask = ld_shared_u32(c.sb + kOffRawMask + rs * 4);
+            float vbound = dequant_tile(c.sb + kOffRaw + rs * kRawStageBytes, c.sb + kOffRawSc + rs * kBK * 8,
+                                        c.sb + kOffX + xs * kXStageBytes, mask, dtid, c.half);
+            if (dtid == 0) st_shared_u32(c.sb + kOffXMask + xs * 4, mask);
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) vbound = fmaxf(vbound, __shfl_xor_sync(0xffffffffu, vbound, o));
-            if (lane == 0)
-                asm volatile("st.shared.f32 [%0], %1;" :: "r"(c.sb + kOffXVmax + (xs * 4 + dw) * 4), "f"(vbound) : "memory");
+            if (lane == 0) st_shared_f32(c.sb + kOffXVmax + (xs * 4 + dw) * 4, vbound);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
@@ -450,31 +477,28 @@ __device__ void dequant_role(const Ctx& c, const UnitDesc* units, int n_units, i
 // ---------------------------------------------------------------------------
 // role: MMA issuer (one thread)
 // ---------------------------------------------------------------------------
-// PV(j): O += P(j) . X(j), with P as the hi then lo bf16 pair from TMEM.
+// PV(j): O += P(j) . X(j) over this CTA's dims, P as the hi then (unless every
+// softmax warp voted to skip it) the lo bf16 half, both from TMEM.
 __device__ __forceinline__ bool issue_pv(const Ctx& c, uint32_t j, bool first_of_unit) {
     const uint32_t sb = j & 1u, xs = j % kNX;
-    if (!wait_bar<false>(c, bar_addr(c, BAR_P_FULL + sb), (j >> 1) & 1u)) return false;
+    if (!wait_bar(c, bar_addr(c, BAR_P_FULL + sb), (j >> 1) & 1u)) return false;
     tc_fence_after();
     const uint32_t idesc_pv = idesc_bf16_f32(128, 256, false, true);
-    const uint32_t xb = c.sb + kOffX + xs * kXStageBytes;
-    const uint32_t tp = c.tmem + kTmemS + sb * 64;
+    const uint32_t xb = c.sb + kOffX + xs * kXStageBytes + c.half * 4 * kAtomBytes;
+    const uint32_t tp = c.tmem + kTmemS + sb * kBK;
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-        const uint64_t bd = sdesc_sw128(xb + kk * 2048, kBK * 128, 1024);
+    for (int kk = 0; kk < kBK / 16; ++kk) {
+        const uint64_t bd = sdesc_sw128(xb + kk * 2048, kAtomBytes, 1024);
         mma_bf16_ts(c.tmem + kTmemO, tp + kk * 8, bd, idesc_pv, (first_of_unit && kk == 0) ? 0u : 1u);
     }
     uint32_t votes = 1u;
 #pragma unroll
-    for (int w = 0; w < kSoftmaxWarps; ++w) {
-        uint32_t v;
-        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(c.sb + kOffVote + (sb * 4 + w) * 4) : "memory");
-        votes &= v;
-    }
+    for (int w = 0; w < kSoftmaxWarps; ++w) votes &= ld_shared_u32(c.sb + kOffVote + (sb * 4 + w) * 4);
     if (votes == 0u) {  // some head needs the lo half of P on this tile
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t bd = sdesc_sw128(xb + kk * 2048, kBK * 128, 1024);
-            mma_bf16_ts(c.tmem + kTmemO, tp + 32 + kk * 8, bd, idesc_pv, 1u);
+        for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint64_t bd = sdesc_sw128(xb + kk * 2048, kAtomBytes, 1024);
+            mma_bf16_ts(c.tmem + kTmemO, tp + kBK / 2 + kk * 8, bd, idesc_pv, 1u);
         }
     }
     mma_commit(bar_addr(c, BAR_X_EMPTY + xs));
@@ -488,19 +512,26 @@ __device__ void mma_role(const Ctx& c, const UnitDesc* units, int n_units) {
     bool ok = true;
     for (int ui = 0; ui < n_units && ok; ++ui) {
         const int n = units[ui].t_end - units[ui].t_begin;
-        if (!wait_bar<false>(c, bar_addr(c, BAR_Q_READY), (uint32_t)ui & 1u)) break;
+        if (!wait_bar(c, bar_addr(c, BAR_Q_READY), (uint32_t)ui & 1u)) break;
         tc_fence_after();
         const uint32_t g0 = g;
         for (int i = 0; i < n; ++i, ++g) {
             const uint32_t xs = g % kNX;
-            if (!wait_bar<false>(c, bar_addr(c, BAR_X_FULL + xs), (g / kNX) & 1u)) { ok = false; break; }
+            if (!wait_bar(c, bar_addr(c, BAR_X_FULL + xs), (g / kNX) & 1u)) { ok = false; break; }
             tc_fence_after();
             const uint32_t xb = c.sb + kOffX + xs * kXStageBytes;
-            const uint32_t ts = c.tmem + kTmemS + (g & 1u) * 64;
+            const uint32_t ts = c.tmem + kTmemS + (g & 1u) * kBK;
+            // K = 512 in 32 steps: dims 0..255 with Q from TMEM, 256..511 with Q from shared memory
 #pragma unroll
             for (int kk = 0; kk < 16; ++kk) {
-                const uint64_t bd = sdesc_sw128(xb + (kk >> 2) * (kBK * 128) + (kk & 3) * 32, 16, 1024);
+                const uint64_t bd = sdesc_sw128(xb + (kk >> 2) * kAtomBytes + (kk & 3) * 32, 16, 1024);
                 mma_bf16_ts(ts, c.tmem + kTmemQ + kk * 8, bd, idesc_qk, kk > 0 ? 1u : 0u);
+            }
+#pragma unroll
+            for (int kk = 16; kk < 32; ++kk) {
+                const uint64_t ad = sdesc_sw128(c.sb + kOffQ + ((kk - 16) >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+                const uint64_t bd = sdesc_sw128(xb + (kk >> 2) * kAtomBytes + (kk & 3) * 32, 16, 1024);
+                mma_bf16_ss(ts, ad, bd, idesc_qk, 1u);
             }
             mma_commit(bar_addr(c, BAR_S_FULL + (g & 1u)));
             if (i > 0 && !issue_pv(c, g - 1, (g - 1) == g0)) { ok = false; break; }
@@ -524,39 +555,40 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, const UnitDesc* uni
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     const float qscale = a.sm_scale * kLog2e;
     const float sink2 = (a.sink != nullptr && h < H) ? __ldg(a.sink + h) * kLog2e : -INFINITY;
-    const uint32_t peer_sin = map_to_rank(c.sb + kOffSin, c.peer);
-    const uint32_t peer_full = map_to_rank(bar_addr(c, BAR_EX_FULL), c.peer);
-    const uint32_t peer_empty = map_to_rank(bar_addr(c, BAR_EX_EMPTY), c.peer);
     volatile uint32_t* flag = reinterpret_cast<volatile uint32_t*>(
         static_cast<uint8_t*>(__cvta_shared_to_generic(c.sb + kOffMisc + 12)));  // misc[3]
-    uint32_t g = 0, pv = 0, ex = 0;
+    uint32_t g = 0, pv = 0;
     bool ok = true;
 
     for (int ui = 0; ui < n_units && ok; ++ui) {
         const UnitDesc d = units[ui];
         const int r = d.row;
         const int n = d.t_end - d.t_begin;
-        // ---- Q half of this row -> TMEM columns [384, 512) (bf16 pairs) ----
+        // ---- Q of this row: dims 0..255 -> TMEM [320, 448) as bf16 pairs,
+        //      dims 256..511 -> shared memory, K-major with the 128-byte swizzle ----
         {
             const size_t hq = (size_t)r * H + (h < H ? h : 0);
             const uint16_t* qn = static_cast<const uint16_t*>(a.q_nope) + hq * SMLA_NOPE_DIMS;
             const uint16_t* qr = static_cast<const uint16_t*>(a.q_rope) + hq * SMLA_ROPE_DIMS;
 #pragma unroll 1
-            for (int cc = 0; cc < 4; ++cc) {  // 4 x 32 columns = 256 dims
+            for (int cc = 0; cc < 4; ++cc) {  // dims 64cc .. 64cc+63 -> 32 TMEM columns
                 uint32_t v[32];
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
-                    const int k = cc * 8 + q;  // 16-byte chunk of this CTA's 256 dims
                     uint4 w = make_uint4(0u, 0u, 0u, 0u);
-                    if (h < H) {
-                        if (c.crank == 0) w = __ldg(reinterpret_cast<const uint4*>(qn + k * 8));
-                        else if (k < 24) w = __ldg(reinterpret_cast<const uint4*>(qn + 256 + k * 8));
-                        else w = __ldg(reinterpret_cast<const uint4*>(qr + (k - 24) * 8));
-                    }
+                    if (h < H) w = __ldg(reinterpret_cast<const uint4*>(qn + (cc * 8 + q) * 8));
                     v[4 * q] = w.x; v[4 * q + 1] = w.y; v[4 * q + 2] = w.z; v[4 * q + 3] = w.w;
                 }
                 tmem_st32(c.tmem + kTmemQ + lane_base + 32 * cc, v);
             }
+#pragma unroll 4
+            for (int k = 0; k < 32; ++k) {  // dims 256 + 8k .. : NoPE 256..447, then RoPE 0..63
+                uint4 w = make_uint4(0u, 0u, 0u, 0u);
+                if (h < H) w = k < 24 ? __ldg(reinterpret_cast<const uint4*>(qn + 256 + k * 8))
+                                      : __ldg(reinterpret_cast<const uint4*>(qr + (k - 24) * 8));
+                st_shared_v4(c.sb + kOffQ + (k >> 3) * 16384 + sw128_offset(h, k & 7), w.x, w.y, w.z, w.w);
+            }
+            fence_proxy_async_smem();
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
@@ -568,62 +600,61 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, const UnitDesc* uni
         bool o_init = false;
         for (int i = 0; i < n; ++i, ++g) {
             const uint32_t sbuf = g & 1u;
-            if (!wait_bar_warp<false>(c, bar_addr(c, BAR_S_FULL + sbuf), (g >> 1) & 1u)) { ok = false; break; }
+            const uint32_t ts = c.tmem + kTmemS + sbuf * kBK + lane_base;
+            if (!wait_bar_warp(c, bar_addr(c, BAR_S_FULL + sbuf), (g >> 1) & 1u)) { ok = false; break; }
+            // The tile's valid mask and |V| bound were written before its X_FULL
+            // arrival; X_FULL of this tile cannot have advanced further (its stage
+            // is refilled only after PV of this tile, which needs this thread's P).
+            if (!wait_bar_warp(c, bar_addr(c, BAR_X_FULL + g % kNX), (g / kNX) & 1u)) { ok = false; break; }
             tc_fence_after();
-            float s[64];
+            const uint32_t vmask = ld_shared_u32(c.sb + kOffXMask + (g % kNX) * 4);
+            float s[kBK];
             {
-                uint32_t v0[32], v1[32];
-                tmem_ld32(c.tmem + kTmemS + sbuf * 64 + lane_base, v0);
-                tmem_ld32(c.tmem + kTmemS + sbuf * 64 + lane_base + 32, v1);
+                uint32_t v[32];
+                tmem_ld32(ts, v);
                 tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < 32; ++j) { s[j] = __uint_as_float(v0[j]); s[32 + j] = __uint_as_float(v1[j]); }
+                for (int j = 0; j < kBK; ++j) s[j] = ((vmask >> j) & 1u) ? __uint_as_float(v[j]) * qscale : -INFINITY;
             }
-            // ---- swap partial scores with the peer CTA ----
-            if (ex > 0 && !wait_bar_warp<true>(c, bar_addr(c, BAR_EX_EMPTY), (ex - 1) & 1u)) { ok = false; break; }
+            float mx[8];
 #pragma unroll
-            for (int q = 0; q < 16; ++q)
-                st_cluster_v4(peer_sin + h * 256 + ((q ^ (h & 15)) << 4), s[4 * q], s[4 * q + 1], s[4 * q + 2], s[4 * q + 3]);
-            mbar_arrive_remote(peer_full);
-            if (!wait_bar_warp<true>(c, bar_addr(c, BAR_EX_FULL), ex & 1u)) { ok = false; break; }
-#pragma unroll
-            for (int q = 0; q < 16; ++q) {
-                const uint4 v = ld_shared_v4(c.sb + kOffSin + h * 256 + ((q ^ (h & 15)) << 4));
-                s[4 * q] += __uint_as_float(v.x);
-                s[4 * q + 1] += __uint_as_float(v.y);
-                s[4 * q + 2] += __uint_as_float(v.z);
-                s[4 * q + 3] += __uint_as_float(v.w);
-            }
-            mbar_arrive_remote(peer_empty);
-            ++ex;
-            // ---- online softmax (log2 domain) with a conditional rescale ----
-            // The tile's valid mask was written before its X_FULL arrival; X_FULL of
-            // this tile cannot have advanced further (its stage is refilled only after
-            // PV of this tile, which needs this thread's P).
-            if (!wait_bar_warp<false>(c, bar_addr(c, BAR_X_FULL + g % kNX), (g / kNX) & 1u)) { ok = false; break; }
-            const uint64_t vmask = ld_shared_u64(c.sb + kOffXMask + (g % kNX) * 8);
-            float mt = -INFINITY;
-#pragma unroll
-            for (int j = 0; j < 64; ++j) {
-                s[j] = ((vmask >> j) & 1ull) ? s[j] * qscale : -INFINITY;
-                mt = fmaxf(mt, s[j]);
-            }
+            for (int j = 0; j < kBK; ++j) mx[j & 7] = (j < 8) ? s[j] : fmaxf(mx[j & 7], s[j]);
+            const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
             float m_new = m_used;
             if (m_used == -INFINITY || mt > m_used + kRescaleThreshold) m_new = fmaxf(m_used, mt);
-            const float alpha = (m_used == -INFINITY) ? 0.f : exp2f(m_used - m_new);
-            float ps = 0.f;
+            const float alpha = (m_used == -INFINITY) ? 0.f : ex2_approx(m_used - m_new);
+            // m_new is finite once any slot was valid; invalid slots give 2^-inf = +0
+            const float msub = (m_new == -INFINITY) ? 0.f : m_new;
+            const bool rescale = o_init && (m_new != m_used);
+            m_used = m_new;
+            // ---- P = 2^(s - m) as a bf16 hi/lo pair, written back over the scores
+            // (hi in columns [0, 16), lo in [16, 32)).  Safe before PV(g-1) completes:
+            // these columns were last read by PV(g-2), which retired before QK(g)
+            // (same issue stream) produced this tile's scores.
+            float ps = 0.f, lo_abs = 0.f;
+            {
+                uint32_t hv[16], lv[16];
+                float sm[4] = {0.f, 0.f, 0.f, 0.f}, la[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int j = 0; j < 64; ++j) {
-                s[j] = (s[j] == -INFINITY) ? 0.f : exp2f(s[j] - m_new);
-                ps += s[j];
+                for (int j = 0; j < 16; ++j) {
+                    const float p0 = ex2_approx(s[2 * j] - msub), p1 = ex2_approx(s[2 * j + 1] - msub);
+                    sm[j & 3] += p0 + p1;
+                    split_bf16x2(p0, p1, hv[j], lv[j]);
+                    const __nv_bfloat162 lb = *reinterpret_cast<const __nv_bfloat162*>(&lv[j]);
+                    la[j & 3] += fabsf(__low2float(lb)) + fabsf(__high2float(lb));
+                }
+                ps = (sm[0] + sm[1]) + (sm[2] + sm[3]);
+                lo_abs = (la[0] + la[1]) + (la[2] + la[3]);
+                tmem_st16(ts, hv);
+                tmem_st16(ts + kBK / 2, lv);
             }
             lsum = lsum * alpha + ps;
             skipped *= alpha;
-            const bool rescale = o_init && (m_new != m_used);
-            m_used = m_new;
-            // PV(g-1) must be done before O is touched or P(g) is handed over
+            // PV(g-1) must be done before O is rescaled (its completion is consumed
+            // once per tile to keep the barrier's phases in step).
             if (i > 0) {
-                if (!wait_bar_warp<false>(c, bar_addr(c, BAR_O_DONE), pv & 1u)) { ok = false; break; }
+                if (!wait_bar_warp(c, bar_addr(c, BAR_O_DONE), pv & 1u)) { ok = false; break; }
                 ++pv;
                 tc_fence_after();
             }
@@ -639,37 +670,17 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, const UnitDesc* uni
                     tmem_st32(c.tmem + kTmemO + lane_base + 32 * cc, v);
                 }
             }
-            // ---- P -> TMEM score columns: hi in [0, 32), lo in [32, 64) ----
-            float lo_abs = 0.f;
-            {
-                uint32_t hi[32], lo[32];
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    split_bf16x2(s[2 * j], s[2 * j + 1], hi[j], lo[j]);
-                    const __nv_bfloat162 hv = *reinterpret_cast<const __nv_bfloat162*>(&hi[j]);
-                    lo_abs += fabsf(s[2 * j] - __low2float(hv)) + fabsf(s[2 * j + 1] - __high2float(hv));
-                }
-                tmem_st32(c.tmem + kTmemS + sbuf * 64 + lane_base, hi);
-                tmem_st32(c.tmem + kTmemS + sbuf * 64 + lane_base + 32, lo);
-            }
-            // vote on skipping the lo half: sum|lo| (x1.01 for its own rounding) x max|V| of the tile
+            // vote on skipping the lo half: sum|lo| x max|V| (this CTA's dims) bounds what skipping drops
             {
                 const uint32_t vb = c.sb + kOffXVmax + (g % kNX) * 16;
-                float vmax;
-                asm volatile("ld.shared.f32 %0, [%1];" : "=f"(vmax) : "r"(vb) : "memory");
+                float vmax = ld_shared_f32(vb);
 #pragma unroll
-                for (int w = 1; w < kNumDequantWarps; ++w) {
-                    float t;
-                    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(t) : "r"(vb + 4 * w) : "memory");
-                    vmax = fmaxf(vmax, t);
-                }
-                const float cand = skipped + lo_abs * 1.0079f * vmax;
+                for (int w = 1; w < kNumDequantWarps; ++w) vmax = fmaxf(vmax, ld_shared_f32(vb + 4 * w));
+                const float cand = skipped + lo_abs * vmax;
                 const bool mine = (h >= H) || (cand <= kLoBudget * lsum);
                 const bool warp_ok = __all_sync(0xffffffffu, mine);
                 if (warp_ok) skipped = cand;  // counted even if another warp vetoes: conservative
-                if (lane == 0)
-                    asm volatile("st.shared.u32 [%0], %1;" :: "r"(c.sb + kOffVote + (sbuf * 4 + warp) * 4),
-                                 "r"(warp_ok ? 1u : 0u) : "memory");
+                if (lane == 0) st_shared_u32(c.sb + kOffVote + (sbuf * 4 + warp) * 4, warp_ok ? 1u : 0u);
             }
             tmem_wait_st();
             tc_fence_before();
@@ -678,7 +689,7 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, const UnitDesc* uni
             o_init = true;
         }
         if (ok && n > 0) {
-            if (!wait_bar_warp<false>(c, bar_addr(c, BAR_O_DONE), pv & 1u)) ok = false;
+            if (!wait_bar_warp(c, bar_addr(c, BAR_O_DONE), pv & 1u)) ok = false;
             ++pv;
             tc_fence_after();
         }
@@ -699,7 +710,7 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, const UnitDesc* uni
                 lse = (M + log2f(Z)) * kLn2;
             }
             if (lsum == 0.f) lse = (a.sink != nullptr && h < H) ? __ldg(a.sink + h) : -INFINITY;  // sink only, exactly
-            uint16_t* outp = static_cast<uint16_t*>(a.out) + ((size_t)r * H + (h < H ? h : 0)) * SMLA_HEAD_DIM + 256 * c.crank;
+            uint16_t* outp = static_cast<uint16_t*>(a.out) + ((size_t)r * H + (h < H ? h : 0)) * SMLA_HEAD_DIM + 256 * c.half;
 #pragma unroll 1
             for (int cc = 0; cc < 8; ++cc) {
                 uint32_t v[32];
@@ -722,10 +733,10 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, const UnitDesc* uni
                     }
                 }
             }
-            if (c.crank == 0 && a.lse != nullptr && h < H) a.lse[(size_t)r * H + h] = lse;
+            if (c.half == 0 && a.lse != nullptr && h < H) a.lse[(size_t)r * H + h] = lse;
         } else {
             const size_t ub = (size_t)d.unit;
-            float* po = p.po + (ub * H + (h < H ? h : 0)) * SMLA_HEAD_DIM + 256 * c.crank;
+            float* po = p.po + (ub * H + (h < H ? h : 0)) * SMLA_HEAD_DIM + 256 * c.half;
 #pragma unroll 1
             for (int cc = 0; cc < 8; ++cc) {
                 uint32_t v[32];
@@ -739,11 +750,11 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, const UnitDesc* uni
                                            __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3])));
                 }
             }
-            if (h < H) __stcg(p.ml + (ub * 2 + c.crank) * H + h, make_float2(m_used, lsum));
+            if (h < H) __stcg(p.ml + (ub * 2 + c.half) * H + h, make_float2(m_used, lsum));
             __threadfence();
             softmax_bar();
             if (h == 0) {
-                const uint32_t old = atomicAdd(p.counters + 2 * r + c.crank, 1u);
+                const uint32_t old = atomicAdd(p.counters + 2 * r + c.half, 1u);
                 *flag = (old == (uint32_t)(d.s_r - 1)) ? 1u : 0u;
             }
             softmax_bar();
@@ -752,18 +763,18 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, const UnitDesc* uni
                 if (h < H) {
                     float M = sink2;
                     for (int i = 0; i < d.s_r; ++i)
-                        M = fmaxf(M, __ldcg(p.ml + ((size_t)(d.row_u0 + i) * 2 + c.crank) * H + h).x);
+                        M = fmaxf(M, __ldcg(p.ml + ((size_t)(d.row_u0 + i) * 2 + c.half) * H + h).x);
                     float Z = 0.f, lall = 0.f;
                     if (M != -INFINITY) {
                         Z = (sink2 == -INFINITY) ? 0.f : exp2f(sink2 - M);
                         for (int i = 0; i < d.s_r; ++i) {
-                            const float2 ml = __ldcg(p.ml + ((size_t)(d.row_u0 + i) * 2 + c.crank) * H + h);
+                            const float2 ml = __ldcg(p.ml + ((size_t)(d.row_u0 + i) * 2 + c.half) * H + h);
                             if (ml.x != -INFINITY) Z += ml.y * exp2f(ml.x - M);
                             lall += ml.y;
                         }
                     }
                     const float inv = Z > 0.f ? 1.f / Z : 0.f;
-                    uint16_t* outp = static_cast<uint16_t*>(a.out) + ((size_t)r * H + h) * SMLA_HEAD_DIM + 256 * c.crank;
+                    uint16_t* outp = static_cast<uint16_t*>(a.out) + ((size_t)r * H + h) * SMLA_HEAD_DIM + 256 * c.half;
 #pragma unroll 1
                     for (int cc = 0; cc < 8; ++cc) {
                         float acc[32];
@@ -771,10 +782,10 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, const UnitDesc* uni
                         for (int j = 0; j < 32; ++j) acc[j] = 0.f;
                         for (int i = 0; i < d.s_r; ++i) {
                             const size_t u = (size_t)(d.row_u0 + i);
-                            const float mi = __ldcg(p.ml + (u * 2 + c.crank) * H + h).x;
+                            const float mi = __ldcg(p.ml + (u * 2 + c.half) * H + h).x;
                             if (mi == -INFINITY) continue;
                             const float w = exp2f(mi - M) * inv;
-                            const float* src = p.po + (u * H + h) * SMLA_HEAD_DIM + 256 * c.crank + 32 * cc;
+                            const float* src = p.po + (u * H + h) * SMLA_HEAD_DIM + 256 * c.half + 32 * cc;
 #pragma unroll
                             for (int q = 0; q < 8; ++q) {
                                 const float4 v = __ldcg(reinterpret_cast<const float4*>(src + 4 * q));
@@ -794,13 +805,13 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, const UnitDesc* uni
                             *reinterpret_cast<uint4*>(outp + 32 * cc + 8 * q) = wv;
                         }
                     }
-                    if (c.crank == 0 && a.lse != nullptr) {
+                    if (c.half == 0 && a.lse != nullptr) {
                         float lse = (M == -INFINITY || Z <= 0.f) ? -INFINITY : (M + log2f(Z)) * kLn2;
                         if (lall == 0.f) lse = a.sink != nullptr ? __ldg(a.sink + h) : -INFINITY;  // sink only, exactly
                         a.lse[(size_t)r * H + h] = lse;
                     }
                 }
-                if (h == 0) atomicExch(p.counters + 2 * r + c.crank, 0u);
+                if (h == 0) atomicExch(p.counters + 2 * r + c.half, 0u);
             }
         }
         // All TMEM reads of O are complete (tcgen05.wait::ld) before the next
@@ -814,32 +825,29 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, const UnitDesc* uni
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-smla_decode_kernel(const KParams p) {
+__global__ void __launch_bounds__(kThreads, 1) smla_decode_kernel(const KParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const smla_decode_args& a = p.a;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     Ctx c;
     c.sb = smem_addr(smem);
-    c.crank = cluster_ctarank();
-    c.peer = c.crank ^ 1u;
+    c.half = blockIdx.x & 1u;
     volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + kOffMisc);
     c.abort = misc + 1;
     long long* red = reinterpret_cast<long long*>(smem + kOffMisc + 64);
-    int* s_tiles = reinterpret_cast<int*>(smem + kOffSin);
+    int* s_tiles = reinterpret_cast<int*>(smem + kOffRaw);  // prologue only
     int* s_prefix = s_tiles + SMLA_MAX_ROWS;
     UnitDesc* units = reinterpret_cast<UnitDesc*>(smem + kOffUnits);
     const int R = a.num_rows;
-    const int cluster = blockIdx.x >> 1;
-    const int n_clusters = gridDim.x >> 1;
+    const int pair = blockIdx.x >> 1;
+    const int n_pairs = gridDim.x >> 1;
 
     uint32_t err = 0;
     if (tid == 0) {
         misc[1] = 0u;
-        mbar_init(bar_addr(c, BAR_Q_READY), kSoftmaxWarps);
         for (int i = 0; i < kNR; ++i) {
-            mbar_init(bar_addr(c, BAR_RAW_FULL + i), 1);
+            mbar_init(bar_addr(c, BAR_RAW_FULL + i), 33);  // 32 async (cp.async) + 1 (producer lane 0)
             mbar_init(bar_addr(c, BAR_RAW_EMPTY + i), kNumDequantWarps);
         }
         for (int i = 0; i < kNX; ++i) {
@@ -851,8 +859,7 @@ smla_decode_kernel(const KParams p) {
             mbar_init(bar_addr(c, BAR_P_FULL + i), kSoftmaxWarps);
         }
         mbar_init(bar_addr(c, BAR_O_DONE), 1);
-        mbar_init(bar_addr(c, BAR_EX_FULL), kHeadsPad);
-        mbar_init(bar_addr(c, BAR_EX_EMPTY), kHeadsPad);
+        mbar_init(bar_addr(c, BAR_Q_READY), kSoftmaxWarps);
         mbar_init(bar_addr(c, BAR_MMA_FINAL), 1);
         fence_mbar_init_cluster();
     }
@@ -862,8 +869,12 @@ smla_decode_kernel(const KParams p) {
     }
 
     // ---- in-kernel split plan (identical in every CTA; reads live lengths) ----
-    // tiles_r per row; smallest chunk c with sum_r max(1, ceil(tiles_r / c)) <= units;
+    // tiles_r per row; smallest chunk c with sum_r max(1, ceil(tiles_r / c)) <= budget;
     // row r gets s_r = ceil(tiles_r / ceil(tiles_r / ceil(tiles_r / c))) splits.
+    // The budget is the caller's rows * num_splits, rounded down to a whole
+    // number of passes over the grid's CTA pairs when it exceeds one pass, so
+    // that no pair is handed one more unit than the others.
+    const int budget = max(R, p.units > n_pairs ? (p.units / n_pairs) * n_pairs : p.units);
     uint32_t plan_err = 0;
     int local_max = 0;
     for (int r = tid; r < R; r += kThreads) {
@@ -890,7 +901,7 @@ smla_decode_kernel(const KParams p) {
         __syncthreads();
         long long tot = 0;
         for (int w = 0; w < kWarps; ++w) tot += red[w];
-        if (tot <= p.units) hi = mid; else lo = mid + 1;
+        if (tot <= budget) hi = mid; else lo = mid + 1;
     }
     const int chunk = lo;
     const int per = (R + kThreads - 1) / kThreads;
@@ -923,10 +934,10 @@ smla_decode_kernel(const KParams p) {
     if (tid == kThreads - 1) s_prefix[R] = run;
     __syncthreads();
     const int total_units = s_prefix[R];
-    // this cluster's units: cluster, cluster + n_clusters, ...
+    // this pair's units: pair, pair + n_pairs, ...
     if (tid == 0) {
         int n = 0;
-        for (int u = cluster; u < total_units && n < kMaxUnitsPerCluster; u += n_clusters, ++n) {
+        for (int u = pair; u < total_units && n < kMaxUnitsPerPair; u += n_pairs, ++n) {
             int l2 = 0, h2 = R - 1;  // last r with prefix[r] <= u
             while (l2 < h2) {
                 const int mid = (l2 + h2 + 1) >> 1;
@@ -948,7 +959,7 @@ smla_decode_kernel(const KParams p) {
     }
     if (blockIdx.x == 0 && plan_err) err |= plan_err;
     tc_fence_before();
-    cluster_sync();  // barrier inits visible to the peer; plan scratch no longer needed
+    __syncthreads();  // barrier inits, TMEM address and unit list visible; plan scratch dead
     tc_fence_after();
     c.tmem = misc[0];
     const int n_units = (int)misc[2];
@@ -957,7 +968,7 @@ smla_decode_kernel(const KParams p) {
         softmax_role(p, c, units, n_units, err);
     } else if (warp < kProducerWarp0 + kNumProducers) {
         producer_role(p, c, units, n_units, warp - kProducerWarp0, err);
-        if (c.crank != 0) err &= ~(SMLA_DEV_BAD_INDEX | SMLA_DEV_BAD_CMP);  // reported once, by CTA 0
+        if (c.half != 0) err &= ~(SMLA_DEV_BAD_INDEX | SMLA_DEV_BAD_CMP);  // reported once, by half 0
     } else if (warp == kMmaWarp) {
         if (lane == 0) mma_role(c, units, n_units);
         __syncwarp();
@@ -973,7 +984,6 @@ smla_decode_kernel(const KParams p) {
         tc_fence_after();
         tmem_dealloc(c.tmem, kTmemCols);
     }
-    cluster_sync();
 }
 
 // ---------------------------------------------------------------------------
@@ -981,7 +991,7 @@ smla_decode_kernel(const KParams p) {
 // ---------------------------------------------------------------------------
 namespace {
 std::atomic<int> g_attr_done[64];
-std::atomic<int> g_num_sms[64];  // co-resident CTA pairs per device
+std::atomic<int> g_resident[64];  // co-resident CTAs of the kernel per device
 std::mutex g_attr_mu;
 
 cudaError_t ensure_kernel_attrs(int dev) {
@@ -991,20 +1001,12 @@ cudaError_t ensure_kernel_attrs(int dev) {
     if (g_attr_done[dev].load(std::memory_order_relaxed) == 1) return cudaSuccess;
     cudaError_t e = cudaFuncSetAttribute(smla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
-    // co-resident CTA pairs of this kernel (cluster placement follows the GPC layout)
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = kSmemBytes;
-    int pairs = 0;
-    e = cudaOccupancyMaxActiveClusters(&pairs, smla_decode_kernel, &cfg);
-    if (e != cudaSuccess || pairs < 1) {
-        int sms = 0;
-        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return e;
-        pairs = sms / 2;
-    }
-    g_num_sms[dev].store(pairs, std::memory_order_relaxed);
+    int per_sm = 0, sms = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, smla_decode_kernel, kThreads, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    g_resident[dev].store(std::max(2, per_sm * sms), std::memory_order_relaxed);
     g_attr_done[dev].store(1, std::memory_order_release);
     return cudaSuccess;
 }
@@ -1023,12 +1025,13 @@ smla_status launch_decode(const smla_decode_args* args, void* workspace, cudaStr
     kp.ml = reinterpret_cast<float2*>(ws + L.off_ml);
     kp.po = reinterpret_cast<float*>(ws + L.off_po);
     kp.units = args->num_rows * args->num_splits;
-    // Persistent grid: one CTA pair per two SMs, at most one pair per unit, and
-    // enough pairs that none is handed more than kMaxUnitsPerCluster units.
-    const int pairs_resident = std::max(1, g_num_sms[dev].load(std::memory_order_relaxed));
-    int clusters = std::min(kp.units, pairs_resident);
-    clusters = std::max(clusters, (kp.units + kMaxUnitsPerCluster - 1) / kMaxUnitsPerCluster);
-    const dim3 grid((unsigned)(2 * clusters)), block(kThreads);
+    // Persistent grid: CTA pairs (one CTA per output half) up to what is
+    // co-resident, at most one pair per unit, and enough pairs that none is
+    // handed more than kMaxUnitsPerPair units.
+    const int pairs_resident = std::max(1, g_resident[dev].load(std::memory_order_relaxed) / 2);
+    int pairs = std::min(kp.units, pairs_resident);
+    pairs = std::max(pairs, (kp.units + kMaxUnitsPerPair - 1) / kMaxUnitsPerPair);
+    const dim3 grid((unsigned)(2 * pairs)), block(kThreads);
     smla_decode_kernel<<<grid, block, kSmemBytes, stream>>>(kp);
     return cudaGetLastError() == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA;
 }
