@@ -23,7 +23,7 @@
 //                        -> 64-bit row; window; compressed) and issue one bulk
 //                        copy per valid entry (576 B) plus a cp.async of its 8
 //                        scale bytes into a 3-stage raw ring;
-//   dequant warps (4)    raw ring -> bf16 (e4m3 x 2^(code-127), exact) in a
+//   dequant warps (8)    raw ring -> bf16 (e4m3 x 2^(code-127), exact) in a
 //                        3-stage ring of 128-byte-swizzled [8 atoms][32][128 B]
 //                        tiles: the K-major B operand of QK and, through the
 //                        atoms of this CTA's dims, the MN-major B of PV;
@@ -65,9 +65,9 @@ constexpr int kSoftmaxWarps = 4;      // warps 0-3: one thread per head
 constexpr int kProducerWarp0 = 4;     // warps 4-6: producer pw owns raw stage pw (tiles g % kNR == pw)
 constexpr int kNumProducers = kNR;    // one per stage: each waits its stage's phases strictly in order
 constexpr int kMmaWarp = 7;
-constexpr int kDequantWarp0 = 8;      // warps 8-11
-constexpr int kNumDequantWarps = 4;
-constexpr int kWarps = 12;
+constexpr int kDequantWarp0 = 8;      // warps 8-15
+constexpr int kNumDequantWarps = 8;
+constexpr int kWarps = 16;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kHeadsPad = 128;        // heads padded up to the MMA M
 static_assert(kHeadsPad == 32 * kSoftmaxWarps, "one softmax thread per padded head");
@@ -98,8 +98,8 @@ constexpr uint32_t kOffRaw = kOffX + kNX * kXStageBytes;        // [kNR][32][576
 constexpr uint32_t kOffRawSc = kOffRaw + kNR * kRawStageBytes;  // [kNR][32] u64 scale codes
 constexpr uint32_t kOffRawMask = kOffRawSc + kNR * kBK * 8;     // [kNR] u32 valid masks
 constexpr uint32_t kOffXMask = kOffRawMask + 16;                // [kNX] u32 valid masks
-constexpr uint32_t kOffXVmax = kOffXMask + 16;                  // [kNX][4 dequant warps] f32 max |V| bound
-constexpr uint32_t kOffVote = kOffXVmax + kNX * 16;             // [2][4 softmax warps] u32 lo-skip votes
+constexpr uint32_t kOffXVmax = kOffXMask + 16;                  // [kNX][8 dequant warps] f32 max |V| bound
+constexpr uint32_t kOffVote = kOffXVmax + kNX * 32;             // [2][4 softmax warps] u32 lo-skip votes
 constexpr uint32_t kOffBar = kOffVote + 32;                     // mbarriers
 constexpr uint32_t kNumBars = 32;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;           // tmem base, flags, reductions
@@ -389,41 +389,47 @@ __device__ void producer_role(const KParams& p, const Ctx& c, const UnitDesc* un
 // ---------------------------------------------------------------------------
 // role: dequant (4 warps): raw ring -> bf16 swizzled tile ring
 // ---------------------------------------------------------------------------
-// Work items: 32 entries x 28 fp8 chunks (16 dims each, atom k/4, UE8M0 group
-// k/4) and 32 entries x 8 bf16 RoPE chunks (atom 7), spread over 128 threads.
-// Every thread loads all of its chunks first, then converts and stores them.
-// It also returns a bound on |x| over the values of this CTA's dims half.
-__device__ __forceinline__ float dequant_tile(uint32_t raw, uint32_t rawsc, uint32_t xb, uint32_t mask, int dtid,
-                                              uint32_t half) {
-    constexpr int kThreadsD = kNumDequantWarps * 32;
-    constexpr int kItems = kBK * 28 / kThreadsD;  // 7
-    constexpr int kRItems = kBK * 8 / kThreadsD;  // 2
-    float vbound = 0.f;
-    uint4 v[kItems];
-    uint32_t code[kItems];
+// Work: 32 entries x 28 fp8 chunks (16 dims each; atom k/4, UE8M0 group k/4)
+// and 32 entries x 8 bf16 RoPE chunks (atom 7).  The fp8 chunks form 28 warp
+// tasks of 8 entries x 4 chunks of one atom (lane: entry lane/4, chunk lane%4),
+// task f handled by dequant warp f % 8; the RoPE chunks form 8 tasks of 4
+// entries x 8 chunks (lane: entry lane/8, chunk lane%8), one per warp.  With
+// these shapes every quarter-warp's 16-byte raw-ring loads (576-byte entry
+// stride) and swizzled tile stores fall in 8 distinct 16-byte bank groups, so
+// neither conflicts.  Each warp loads all of its chunks first, then converts
+// and stores them.  Returns a bound on |x| over the values of this CTA's dims
+// half that this thread wrote.
+static_assert(kNumDequantWarps == 8, "task split below assumes 8 dequant warps");
+constexpr int kFp8Tasks = 28;  // 4 entry groups x 7 atoms
+
+__device__ __forceinline__ float dequant_tile(uint32_t raw, uint32_t rawsc, uint32_t xb, uint32_t mask, int dw,
+                                              int lane, uint32_t half) {
+    // fp8 tasks dw, dw + 8, dw + 16 (all warps) and dw + 24 (warps 0-3 only)
+    const bool has4 = dw + 24 < kFp8Tasks;
+    const int ef = 8 * (dw & 3) + (lane >> 2);  // entry of every fp8 task of this warp (task % 4 == dw % 4)
+    const bool fvalid = (mask >> (ef & 31)) & 1u;
+    uint4 v[4];
+    uint32_t code[4];
 #pragma unroll
-    for (int it = 0; it < kItems; ++it) {
-        const int idx = dtid + it * kThreadsD;
-        const int e = idx / 28, k = idx % 28;
+    for (int it = 0; it < 4; ++it) {
+        const int k = 4 * ((dw + 8 * it) >> 2) + (lane & 3);
         v[it] = make_uint4(0u, 0u, 0u, 0u);
         code[it] = 127u;
-        if ((mask >> e) & 1u) {
-            v[it] = ld_shared_v4(raw + e * SMLA_ENTRY_BYTES + 16 * k);
-            code[it] = ld_shared_u8(rawsc + e * 8 + (k >> 2));
+        if (fvalid && (it < 3 || has4)) {
+            v[it] = ld_shared_v4(raw + ef * SMLA_ENTRY_BYTES + 16 * k);
+            code[it] = ld_shared_u8(rawsc + ef * 8 + (k >> 2));
         }
     }
-    uint4 rv[kRItems];
+    const int er = 4 * dw + (lane >> 3), kr = lane & 7;  // RoPE task dw
+    const bool rvalid = (mask >> (er & 31)) & 1u;
+    uint4 rv = make_uint4(0u, 0u, 0u, 0u);
+    if (rvalid) rv = ld_shared_v4(raw + er * SMLA_ENTRY_BYTES + SMLA_NOPE_DIMS + 16 * kr);
+
+    float vbound = 0.f;
 #pragma unroll
-    for (int it = 0; it < kRItems; ++it) {
-        const int idx = dtid + it * kThreadsD;
-        const int e = idx >> 3, k = idx & 7;
-        rv[it] = make_uint4(0u, 0u, 0u, 0u);
-        if ((mask >> e) & 1u) rv[it] = ld_shared_v4(raw + e * SMLA_ENTRY_BYTES + SMLA_NOPE_DIMS + 16 * k);
-    }
-#pragma unroll
-    for (int it = 0; it < kItems; ++it) {
-        const int idx = dtid + it * kThreadsD;
-        const int e = idx / 28, k = idx % 28;
+    for (int it = 0; it < 4; ++it) {
+        if (it == 3 && !has4) break;
+        const int k = 4 * ((dw + 8 * it) >> 2) + (lane & 3);
         const float scale = ue8m0_to_f32(code[it]);
         uint32_t o[8];
         dequant16(v[it], scale, o);
@@ -433,16 +439,11 @@ __device__ __forceinline__ float dequant_tile(uint32_t raw, uint32_t rawsc, uint
         }
         const uint32_t dst = xb + (k >> 2) * kAtomBytes;
         const int kk = (k & 3) * 2;
-        st_shared_v4(dst + sw128_offset(e, kk), o[0], o[1], o[2], o[3]);
-        st_shared_v4(dst + sw128_offset(e, kk + 1), o[4], o[5], o[6], o[7]);
+        st_shared_v4(dst + sw128_offset(ef, kk), o[0], o[1], o[2], o[3]);
+        st_shared_v4(dst + sw128_offset(ef, kk + 1), o[4], o[5], o[6], o[7]);
     }
-#pragma unroll
-    for (int it = 0; it < kRItems; ++it) {
-        const int idx = dtid + it * kThreadsD;
-        const int e = idx >> 3, k = idx & 7;
-        if (half == 1u) vbound = fmaxf(vbound, bf16x8_absmax(rv[it]));
-        st_shared_v4(xb + 7 * kAtomBytes + sw128_offset(e, k), rv[it].x, rv[it].y, rv[it].z, rv[it].w);
-    }
+    if (half == 1u) vbound = fmaxf(vbound, bf16x8_absmax(rv));
+    st_shared_v4(xb + 7 * kAtomBytes + sw128_offset(er, kr), rv.x, rv.y, rv.z, rv.w);
     return vbound;
 }
 
@@ -459,11 +460,11 @@ __device__ void dequant_role(const Ctx& c, const UnitDesc* units, int n_units, i
             if (!wait_bar_warp(c, bar_addr(c, BAR_X_EMPTY + xs), xph ^ 1u)) return;
             const uint32_t mask = ld_shared_u32(c.sb + kOffRawMask + rs * 4);
             float vbound = dequant_tile(c.sb + kOffRaw + rs * kRawStageBytes, c.sb + kOffRawSc + rs * kBK * 8,
-                                        c.sb + kOffX + xs * kXStageBytes, mask, dtid, c.half);
+                                        c.sb + kOffX + xs * kXStageBytes, mask, dw, lane, c.half);
             if (dtid == 0) st_shared_u32(c.sb + kOffXMask + xs * 4, mask);
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) vbound = fmaxf(vbound, __shfl_xor_sync(0xffffffffu, vbound, o));
-            if (lane == 0) st_shared_f32(c.sb + kOffXVmax + (xs * 4 + dw) * 4, vbound);
+            if (lane == 0) st_shared_f32(c.sb + kOffXVmax + (xs * kNumDequantWarps + dw) * 4, vbound);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
@@ -672,7 +673,7 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, const UnitDesc* uni
             }
             // vote on skipping the lo half: sum|lo| x max|V| (this CTA's dims) bounds what skipping drops
             {
-                const uint32_t vb = c.sb + kOffXVmax + (g % kNX) * 16;
+                const uint32_t vb = c.sb + kOffXVmax + (g % kNX) * (4 * kNumDequantWarps);
                 float vmax = ld_shared_f32(vb);
 #pragma unroll
                 for (int w = 1; w < kNumDequantWarps; ++w) vmax = fmaxf(vmax, ld_shared_f32(vb + 4 * w));
