@@ -16,20 +16,24 @@
 // hold bit-identical scores and make identical softmax decisions, and no data
 // crosses SMs (moving partial scores between SMs through distributed shared
 // memory measured ~2.5 us per 32 KB, several times the tensor time of a tile).
-// The grid is persistent.  Inside a CTA, warp roles pass 32-entry tiles along
-// mbarrier rings:
+// The grid is persistent.  Inside a CTA, warp roles pass tiles along
+// mbarrier rings.  A tile is 64 entries (the N of QK: a tcgen05 MMA with
+// M = 128 costs about the same for N = 32 and N = 64, so 64 halves the QK
+// cost per entry); entries are fetched in 32-entry raw tiles, two per tile.
 //
-//   producer warps (3)   one per raw stage: resolve a tile's 32 slots (top-k index -> page table
-//                        -> 64-bit row; window; compressed) and issue one bulk
-//                        copy per valid entry (576 B) plus a cp.async of its 8
-//                        scale bytes into a 3-stage raw ring;
-//   dequant warps (8)    raw ring -> bf16 (e4m3 x 2^(code-127), exact) in a
-//                        3-stage ring of 128-byte-swizzled [8 atoms][32][128 B]
-//                        tiles: the K-major B operand of QK and, through the
-//                        atoms of this CTA's dims, the MN-major B of PV;
-//   MMA warp (1 thread)  QK(t): M = 128 heads, N = 32, K = 512 with Q dims
+//   producer warps (3)   one per raw stage: resolve a raw tile's 32 slots (top-k index -> page
+//                        table -> 64-bit row; window; compressed) and issue one
+//                        bulk copy per valid entry (576 B) plus a cp.async of
+//                        its 8 scale bytes into a 3-stage raw ring;
+//   dequant warps (8)    raw ring -> bf16 (e4m3 x 2^(code-127), exact) in
+//                        128-byte-swizzled [4 atoms][64][128 B] halves of a
+//                        tile: this CTA's 256 dims ("own": the K-major B of QK
+//                        and the MN-major B of PV) in a 2-stage ring, the other
+//                        256 dims ("peer": QK only) in a single stage that is
+//                        refilled as soon as QK of the previous tile is done;
+//   MMA warp (1 thread)  QK(t): M = 128 heads, N = 64, K = 512 with Q dims
 //                        0..255 from TMEM and 256..511 from shared memory;
-//                        then PV(t-1): M = 128, N = 256, K = 32 with P from TMEM;
+//                        then PV(t-1): M = 128, N = 256, K = 64 with P from TMEM;
 //   softmax warps (4)    one thread per head (TMEM lane): online softmax with a
 //                        conditional rescale, P written back over the scores as
 //                        a bf16 pair hi = bf16(p), lo = bf16(p - hi).  A single
@@ -40,9 +44,9 @@
 //                        its total effect on every head's output stays within
 //                        2^-9; on peaked softmaxes most tiles qualify.
 //
-// TMEM (512 columns): O [0, 256), two score/P buffers [256, 320), Q dims
-// 0..255 as bf16 pairs [320, 448).  Heads beyond num_heads are zero-padded up
-// to the MMA's M = 128.
+// TMEM (512 columns): O [0, 256), two score/P buffers [256, 320) and
+// [320, 384), Q dims 0..255 as bf16 pairs [384, 512).  Heads beyond num_heads
+// are zero-padded up to the MMA's M = 128.
 #include <algorithm>
 #include <cstdint>
 #include <cstring>
@@ -58,9 +62,11 @@
 
 namespace smla {
 
-constexpr int kBK = 32;               // entries per tile
+constexpr int kBK = 64;               // entries per tile (QK N, PV K)
+constexpr int kRawBK = 32;            // entries per raw tile (one producer lane each)
+constexpr int kRawPerTile = kBK / kRawBK;
 constexpr int kNR = 3;                // raw-byte ring stages
-constexpr int kNX = 3;                // bf16 tile ring stages
+constexpr int kNXO = 2;               // own-dims tile stages
 constexpr int kSoftmaxWarps = 4;      // warps 0-3: one thread per head
 constexpr int kProducerWarp0 = 4;     // warps 4-6: producer pw owns raw stage pw (tiles g % kNR == pw)
 constexpr int kNumProducers = kNR;    // one per stage: each waits its stage's phases strictly in order
@@ -71,13 +77,13 @@ constexpr int kWarps = 16;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kHeadsPad = 128;        // heads padded up to the MMA M
 static_assert(kHeadsPad == 32 * kSoftmaxWarps, "one softmax thread per padded head");
-static_assert(kBK == 32, "one producer lane per slot");
+static_assert(kRawBK == 32, "one producer lane per slot");
 constexpr int kMaxUnitsPerPair = 32;
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;        // O half: columns [0, 256)
-constexpr uint32_t kTmemS = 256;      // score / P buffers: [256, 288), [288, 320)
-constexpr uint32_t kTmemQ = 320;      // Q dims 0..255, bf16 packed: [320, 448)
+constexpr uint32_t kTmemS = 256;      // score / P buffers: [256, 320), [320, 384)
+constexpr uint32_t kTmemQ = 384;      // Q dims 0..255, bf16 packed: [384, 512)
 constexpr uint64_t kWaitNs = 2000000000ull;  // bounded-wait limit (2 s)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -87,19 +93,20 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: P may grow to 2^8 befo
 // denominator: the output error from skipping is then at most kLoBudget.
 constexpr float kLoBudget = 1.0f / 512.0f;
 
-constexpr uint32_t kAtomBytes = kBK * 128;                   // one 64-dim atom of a tile: 4 KB
-constexpr uint32_t kXStageBytes = 8 * kAtomBytes;            // 32 KB
-constexpr uint32_t kRawStageBytes = kBK * SMLA_ENTRY_BYTES;  // 18 KB
+constexpr uint32_t kAtomBytes = kBK * 128;                      // one 64-dim atom of a tile: 8 KB
+constexpr uint32_t kHalfBytes = 4 * kAtomBytes;                 // 256 dims of a tile: 32 KB
+constexpr uint32_t kRawStageBytes = kRawBK * SMLA_ENTRY_BYTES;  // 18 KB
 
 // Shared-memory layout (offsets from a 1024-byte-aligned base).
-constexpr uint32_t kOffQ = 0;                                   // Q dims 256..511: [4 atoms][128][128 B]
-constexpr uint32_t kOffX = kOffQ + 65536;                       // [kNX][8 atoms][32][128 B]
-constexpr uint32_t kOffRaw = kOffX + kNX * kXStageBytes;        // [kNR][32][576 B]
-constexpr uint32_t kOffRawSc = kOffRaw + kNR * kRawStageBytes;  // [kNR][32] u64 scale codes
-constexpr uint32_t kOffRawMask = kOffRawSc + kNR * kBK * 8;     // [kNR] u32 valid masks
-constexpr uint32_t kOffXMask = kOffRawMask + 16;                // [kNX] u32 valid masks
-constexpr uint32_t kOffXVmax = kOffXMask + 16;                  // [kNX][8 dequant warps] f32 max |V| bound
-constexpr uint32_t kOffVote = kOffXVmax + kNX * 32;             // [2][4 softmax warps] u32 lo-skip votes
+constexpr uint32_t kOffQ = 0;                                      // Q dims 256..511: [4 atoms][128][128 B]
+constexpr uint32_t kOffXO = kOffQ + 65536;                         // own dims: [kNXO][4 atoms][64][128 B]
+constexpr uint32_t kOffXP = kOffXO + kNXO * kHalfBytes;            // peer dims: [4 atoms][64][128 B]
+constexpr uint32_t kOffRaw = kOffXP + kHalfBytes;                  // [kNR][32][576 B]
+constexpr uint32_t kOffRawSc = kOffRaw + kNR * kRawStageBytes;     // [kNR][32] u64 scale codes
+constexpr uint32_t kOffRawMask = kOffRawSc + kNR * kRawBK * 8;     // [kNR] u32 valid masks
+constexpr uint32_t kOffXMask = kOffRawMask + 16;                   // [kNXO][2] u32 valid masks (64 entries)
+constexpr uint32_t kOffXVmax = kOffXMask + kNXO * 8;               // [kNXO][8 dequant warps] f32 max |V| bound
+constexpr uint32_t kOffVote = kOffXVmax + kNXO * 32;               // [2][4 softmax warps] u32 lo-skip votes
 constexpr uint32_t kOffBar = kOffVote + 32;                     // mbarriers
 constexpr uint32_t kNumBars = 32;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;           // tmem base, flags, reductions
@@ -116,9 +123,10 @@ static_assert(4 * (2 * SMLA_MAX_ROWS + 8) <= kNR * kRawStageBytes, "plan scratch
 enum : uint32_t {
     BAR_RAW_FULL = 0,                      // [kNR] producer -> dequant (32 async + 1 arrival, tx bytes)
     BAR_RAW_EMPTY = BAR_RAW_FULL + kNR,    // [kNR] dequant -> producer (kNumDequantWarps)
-    BAR_X_FULL = BAR_RAW_EMPTY + kNR,      // [kNX] dequant -> MMA, softmax (kNumDequantWarps)
-    BAR_X_EMPTY = BAR_X_FULL + kNX,        // [kNX] MMA commit after PV
-    BAR_S_FULL = BAR_X_EMPTY + kNX,        // [2] MMA commit after QK
+    BAR_X_FULL = BAR_RAW_EMPTY + kNR,      // [kNXO] dequant -> MMA, softmax (kNumDequantWarps)
+    BAR_XO_EMPTY = BAR_X_FULL + kNXO,      // [kNXO] MMA commit after PV (own dims free)
+    BAR_XP_EMPTY = BAR_XO_EMPTY + kNXO,    // MMA commit after QK (peer dims free)
+    BAR_S_FULL = BAR_XP_EMPTY + 1,         // [2] MMA commit after QK
     BAR_P_FULL = BAR_S_FULL + 2,           // [2] softmax -> MMA (kSoftmaxWarps)
     BAR_O_DONE = BAR_P_FULL + 2,           // MMA commit after each PV
     BAR_Q_READY = BAR_O_DONE + 1,          // softmax -> MMA, once per unit (kSoftmaxWarps)
@@ -185,6 +193,53 @@ __device__ __forceinline__ void dequant16(const uint4 raw, float scale, uint32_t
     }
 }
 
+// The same conversion by bit placement.  Moving an e4m3 code's 7 magnitude
+// bits to bf16 bits 4..10 and its sign to bit 15 gives a bf16 that reads
+// exactly 2^-120 times the e4m3 value (normal codes land on normal bf16
+// numbers, subnormal codes on bf16 subnormals with the same factor).  One
+// bf16x2 multiply by 2^(code - 7) then yields e4m3 x 2^(code - 127) exactly
+// whenever the product is a normal bf16: scale codes 10..134.  A NaN byte
+// (magnitude 0x7F) comes out as the finite 480 x 2^(code - 127), above the
+// largest e4m3 value 448; fast_chunk_bad() flags both cases.
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, 0, %2;" : "=r"(d) : "r"(a), "r"(sel));
+    return d;
+}
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+// Elementwise max of |a|, |b| (the sign of the result is not used).
+__device__ __forceinline__ uint32_t max_abs_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ void dequant16_fast(const uint4 raw, uint32_t code, uint32_t (&o)[8]) {
+    const uint32_t scale2 = ((code + 120u) << 7) * 0x00010001u;  // bf16x2 of 2^(code - 7)
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        // bytes 0,1 (then 2,3), each followed by a byte of copies of its sign bit
+        const uint32_t lo = prmt(w[i], 0x9180u), hi = prmt(w[i], 0xB3A2u);
+        o[2 * i] = mul_bf16x2((lo << 4) & 0x87F087F0u, scale2);
+        o[2 * i + 1] = mul_bf16x2((hi << 4) & 0x87F087F0u, scale2);
+    }
+}
+// Largest |x| over 8 packed bf16 words, as the 15 magnitude bits of a bf16.
+__device__ __forceinline__ uint32_t absmax_bits8(const uint32_t (&o)[8]) {
+    const uint32_t m = max_abs_bf16x2(max_abs_bf16x2(max_abs_bf16x2(o[0], o[1]), max_abs_bf16x2(o[2], o[3])),
+                                      max_abs_bf16x2(max_abs_bf16x2(o[4], o[5]), max_abs_bf16x2(o[6], o[7])));
+    return max(m & 0x7FFFu, (m >> 16) & 0x7FFFu);
+}
+// True when dequant16_fast's output for this chunk is not the exact one: a
+// scale code outside 10..134, or a NaN byte (a magnitude above 448 x scale).
+__device__ __forceinline__ bool fast_chunk_bad(uint32_t code, uint32_t amax_bits) {
+    return code - 10u > 124u || amax_bits > (((code + 8u) << 7) | 0x60u);
+}
+
 // Upper bound of |x| over 16 e4m3 codes: the 7-bit magnitude pattern of an
 // e4m3 code orders like its value, so the largest pattern decodes to the
 // largest magnitude.  The NaN pattern (0x7F) gives +inf (never skip).
@@ -223,20 +278,22 @@ __device__ __forceinline__ long long map_position(const smla_decode_args& a, lon
     return phys < a.n_main ? phys : -1;
 }
 
-// Number of 64-entry tiles of row r: top-k slots, window, compressed groups.
+// Number of 64-entry tiles of row r.  Its slots are the top-k slots, the
+// window and the compressed entries, each segment padded to 32-entry raw
+// tiles; two raw tiles make a tile (the last one may be half empty).
 __device__ __forceinline__ int row_tiles(const smla_decode_args& a, int r, uint32_t& err) {
-    int t = ceil_div_i(a.topk, kBK);
+    int t = ceil_div_i(a.topk, kRawBK);
     if (a.swa_len != nullptr) {
         int w = __ldg(a.swa_len + r);
         if (w < 0) { err |= SMLA_DEV_BAD_LENGTH; w = 0; }
-        t += ceil_div_i(w, kBK);
+        t += ceil_div_i(w, kRawBK);
     }
     if (a.cmp_len != nullptr) {
         int c = __ldg(a.cmp_len + r);
         if (c < 0) { err |= SMLA_DEV_BAD_LENGTH; c = 0; }
-        t += ceil_div_i(c, kBK);
+        t += ceil_div_i(c, kRawBK);
     }
-    return t;
+    return ceil_div_i(t, kRawPerTile);
 }
 
 // Per-CTA state shared by the roles.
@@ -311,33 +368,35 @@ __device__ __forceinline__ bool softmax_all(bool v) {
 }
 
 // ---------------------------------------------------------------------------
-// role: producer (warp pw owns raw stage pw: tiles g % kNR == pw; lane = slot).
-// A parity wait cannot tell "two phases ahead" from "previous phase done", so
-// each stage has exactly one producer, which waits its phases in order.
+// role: producer (warp pw owns raw stage pw: raw tiles q % kNR == pw, where q
+// counts this CTA's raw tiles, two per tile; lane = slot).  A parity wait
+// cannot tell "two phases ahead" from "previous phase done", so each stage
+// has exactly one producer, which waits its phases in order.
 // ---------------------------------------------------------------------------
 __device__ void producer_role(const KParams& p, const Ctx& c, const UnitDesc* units, int n_units, int pw,
                               uint32_t& err) {
     const smla_decode_args& a = p.a;
     const int lane = threadIdx.x & 31;
-    uint32_t g = 0;
+    uint32_t q = 0;
     for (int ui = 0; ui < n_units; ++ui) {
         const UnitDesc d = units[ui];
         const int r = d.row;
         const int seq = a.row_seq != nullptr ? __ldg(a.row_seq + r) : r;
-        const int nmt = ceil_div_i(a.topk, kBK);
+        const int nmt = ceil_div_i(a.topk, kRawBK);
         int swa_len = 0, swa_start = 0, cmp_len = 0;
         long long cmp_start = 0;
         if (a.swa_len != nullptr) { swa_len = max(0, __ldg(a.swa_len + r)); swa_start = __ldg(a.swa_start + r); }
         if (a.cmp_len != nullptr) { cmp_len = max(0, __ldg(a.cmp_len + r)); cmp_start = __ldg(a.cmp_start + r); }
-        const int nst = ceil_div_i(swa_len, kBK);
-        for (int t = d.t_begin; t < d.t_end; ++t, ++g) {
-            if ((int)(g % kNR) != pw) continue;
-            const uint32_t rs = g % kNR, rph = (g / kNR) & 1u;
-            // resolve this lane's slot
+        const int nst = ceil_div_i(swa_len, kRawBK);
+        const int nct = ceil_div_i(cmp_len, kRawBK);
+        for (int t = kRawPerTile * d.t_begin; t < kRawPerTile * d.t_end; ++t, ++q) {
+            if ((int)(q % kNR) != pw) continue;
+            const uint32_t rs = q % kNR, rph = (q / kNR) & 1u;
+            // resolve this lane's slot (raw tiles past the row's end stay empty)
             long long phys = -1;
             bool cmp = false;
             if (t < nmt) {
-                const int j = t * kBK + lane;
+                const int j = t * kRawBK + lane;
                 if (j < a.topk) {
                     const int idx = __ldg(a.main_idx + (size_t)r * a.topk + j);
                     if (idx != -1) {
@@ -346,13 +405,13 @@ __device__ void producer_role(const KParams& p, const Ctx& c, const UnitDesc* un
                     }
                 }
             } else if (t < nmt + nst) {
-                const int j = (t - nmt) * kBK + lane;
+                const int j = (t - nmt) * kRawBK + lane;
                 if (j < swa_len) {
                     phys = map_position(a, (long long)swa_start + j, seq);
                     if (phys < 0) err |= SMLA_DEV_BAD_INDEX;
                 }
-            } else {
-                const int j = (t - nmt - nst) * kBK + lane;
+            } else if (t < nmt + nst + nct) {
+                const int j = (t - nmt - nst) * kRawBK + lane;
                 if (j < cmp_len) {
                     cmp = true;
                     phys = cmp_start + j;
@@ -375,7 +434,7 @@ __device__ void producer_role(const KParams& p, const Ctx& c, const UnitDesc* un
             __syncwarp();
             if (ep != nullptr) {
                 bulk_g2s(c.sb + kOffRaw + rs * kRawStageBytes + lane * SMLA_ENTRY_BYTES, ep, SMLA_ENTRY_BYTES, full);
-                cp_async_8(c.sb + kOffRawSc + (rs * kBK + lane) * 8, sp);
+                cp_async_8(c.sb + kOffRawSc + (rs * kRawBK + lane) * 8, sp);
             }
             cp_async_arrive_noinc(full);  // one of the 32 async arrivals
             if (lane == 0) {
@@ -387,90 +446,136 @@ __device__ void producer_role(const KParams& p, const Ctx& c, const UnitDesc* un
 }
 
 // ---------------------------------------------------------------------------
-// role: dequant (4 warps): raw ring -> bf16 swizzled tile ring
+// role: dequant (8 warps): raw ring -> bf16 swizzled tile halves
 // ---------------------------------------------------------------------------
-// Work: 32 entries x 28 fp8 chunks (16 dims each; atom k/4, UE8M0 group k/4)
-// and 32 entries x 8 bf16 RoPE chunks (atom 7).  The fp8 chunks form 28 warp
-// tasks of 8 entries x 4 chunks of one atom (lane: entry lane/4, chunk lane%4),
-// task f handled by dequant warp f % 8; the RoPE chunks form 8 tasks of 4
-// entries x 8 chunks (lane: entry lane/8, chunk lane%8), one per warp.  With
-// these shapes every quarter-warp's 16-byte raw-ring loads (576-byte entry
-// stride) and swizzled tile stores fall in 8 distinct 16-byte bank groups, so
-// neither conflicts.  Each warp loads all of its chunks first, then converts
-// and stores them.  Returns a bound on |x| over the values of this CTA's dims
-// half that this thread wrote.
-static_assert(kNumDequantWarps == 8, "task split below assumes 8 dequant warps");
-constexpr int kFp8Tasks = 28;  // 4 entry groups x 7 atoms
-
-__device__ __forceinline__ float dequant_tile(uint32_t raw, uint32_t rawsc, uint32_t xb, uint32_t mask, int dw,
-                                              int lane, uint32_t half) {
-    // fp8 tasks dw, dw + 8, dw + 16 (all warps) and dw + 24 (warps 0-3 only)
-    const bool has4 = dw + 24 < kFp8Tasks;
-    const int ef = 8 * (dw & 3) + (lane >> 2);  // entry of every fp8 task of this warp (task % 4 == dw % 4)
+// A raw tile (32 entries) fills rows [32 k, 32 k + 32) of a tile, k = 0, 1.
+// Its dims split in two sets of 4 atoms: set 0 = fp8 dims 0..255 (atoms
+// 0..3), set 1 = fp8 dims 256..447 (atoms 4..6) and the bf16 RoPE (atom 7).
+// An fp8 warp task is 8 entries x 4 chunks of 16 dims of one atom (lane:
+// entry lane/4, chunk lane%4); a RoPE task is 4 entries x 8 chunks (lane:
+// entry lane/8, chunk lane%8).  With these shapes every quarter-warp's
+// 16-byte raw-ring loads (576-byte entry stride) and swizzled stores fall in 8
+// distinct 16-byte bank groups.  Per set and raw tile each warp takes:
+//   set 0: fp8 (atom dw/4, entry group dw%4) and (atom 2 + dw/4, group dw%4);
+//   set 1: warps 0-3 fp8 (atom 4, group dw) and (atom 6, group dw),
+//          warps 4-7 fp8 (atom 5, group dw-4) and RoPE tasks 2(dw-4), 2(dw-4)+1.
+// A set is written to the 4-atom buffer `dst` (local atom = atom % 4).
+// Returns, when `bound` is set, a bound on |x| over the values written.
+__device__ __forceinline__ float dequant_set(uint32_t raw, uint32_t rawsc, uint32_t dst, int row0, uint32_t mask,
+                                             int set, int dw, int lane, bool bound) {
+    const int ef = 8 * (dw & 3) + (lane >> 2);  // entry of this warp's fp8 tasks
     const bool fvalid = (mask >> (ef & 31)) & 1u;
-    uint4 v[4];
-    uint32_t code[4];
+    int atom[2];
+    if (set == 0) { atom[0] = dw >> 2; atom[1] = 2 + (dw >> 2); }
+    else { atom[0] = dw < 4 ? 4 : 5; atom[1] = 6; }
+    const bool second_fp8 = set == 0 || dw < 4;
+    uint4 v[2];
+    uint32_t code[2];
 #pragma unroll
-    for (int it = 0; it < 4; ++it) {
-        const int k = 4 * ((dw + 8 * it) >> 2) + (lane & 3);
+    for (int it = 0; it < 2; ++it) {
+        const int k = 4 * atom[it] + (lane & 3);
         v[it] = make_uint4(0u, 0u, 0u, 0u);
         code[it] = 127u;
-        if (fvalid && (it < 3 || has4)) {
+        if (fvalid && (it == 0 || second_fp8)) {
             v[it] = ld_shared_v4(raw + ef * SMLA_ENTRY_BYTES + 16 * k);
-            code[it] = ld_shared_u8(rawsc + ef * 8 + (k >> 2));
+            code[it] = ld_shared_u8(rawsc + ef * 8 + atom[it]);
         }
     }
-    const int er = 4 * dw + (lane >> 3), kr = lane & 7;  // RoPE task dw
-    const bool rvalid = (mask >> (er & 31)) & 1u;
-    uint4 rv = make_uint4(0u, 0u, 0u, 0u);
-    if (rvalid) rv = ld_shared_v4(raw + er * SMLA_ENTRY_BYTES + SMLA_NOPE_DIMS + 16 * kr);
-
-    float vbound = 0.f;
+    const bool has_rope = !second_fp8;
+    uint4 rv[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
+    const int kr = lane & 7;
+    int er[2];
 #pragma unroll
-    for (int it = 0; it < 4; ++it) {
-        if (it == 3 && !has4) break;
-        const int k = 4 * ((dw + 8 * it) >> 2) + (lane & 3);
-        const float scale = ue8m0_to_f32(code[it]);
+    for (int it = 0; it < 2; ++it) {
+        er[it] = 4 * (2 * (dw - 4) + it) + (lane >> 3);
+        if (has_rope && ((mask >> (er[it] & 31)) & 1u))
+            rv[it] = ld_shared_v4(raw + er[it] * SMLA_ENTRY_BYTES + SMLA_NOPE_DIMS + 16 * kr);
+    }
+
+    // straight-line fast path for every chunk; the rare chunks it gets wrong
+    // are redone below with the exact conversion
+    uint32_t amax = 0u;
+    bool bad[2] = {false, false};
+    const int kk = (lane & 3) * 2;
+#pragma unroll
+    for (int it = 0; it < 2; ++it) {
+        if (it == 1 && !second_fp8) break;
         uint32_t o[8];
-        dequant16(v[it], scale, o);
-        if ((uint32_t)(k >> 4) == half) {  // dims 16k.. lie in this CTA's half
+        dequant16_fast(v[it], code[it], o);
+        const uint32_t am = absmax_bits8(o);
+        bad[it] = fast_chunk_bad(code[it], am);
+        amax = max(amax, am);
+        const uint32_t d = dst + (atom[it] & 3) * kAtomBytes;
+        st_shared_v4(d + sw128_offset(row0 + ef, kk), o[0], o[1], o[2], o[3]);
+        st_shared_v4(d + sw128_offset(row0 + ef, kk + 1), o[4], o[5], o[6], o[7]);
+    }
+    float vbound = __uint_as_float(amax << 16);
+    if (has_rope) {
+#pragma unroll
+        for (int it = 0; it < 2; ++it) {
+            if (bound) vbound = fmaxf(vbound, bf16x8_absmax(rv[it]));
+            st_shared_v4(dst + 3 * kAtomBytes + sw128_offset(row0 + er[it], kr), rv[it].x, rv[it].y, rv[it].z, rv[it].w);
+        }
+    }
+    if (__any_sync(0xffffffffu, bad[0] || bad[1])) {
+#pragma unroll
+        for (int it = 0; it < 2; ++it) {
+            if (!bad[it]) continue;
+            const float scale = ue8m0_to_f32(code[it]);
+            uint32_t o[8];
+            dequant16(v[it], scale, o);
             const float bnd = e4m3x16_absmax(v[it]) * scale;
             vbound = (bnd > vbound || bnd != bnd) ? (bnd != bnd ? INFINITY : bnd) : vbound;
+            const uint32_t d = dst + (atom[it] & 3) * kAtomBytes;
+            st_shared_v4(d + sw128_offset(row0 + ef, kk), o[0], o[1], o[2], o[3]);
+            st_shared_v4(d + sw128_offset(row0 + ef, kk + 1), o[4], o[5], o[6], o[7]);
         }
-        const uint32_t dst = xb + (k >> 2) * kAtomBytes;
-        const int kk = (k & 3) * 2;
-        st_shared_v4(dst + sw128_offset(ef, kk), o[0], o[1], o[2], o[3]);
-        st_shared_v4(dst + sw128_offset(ef, kk + 1), o[4], o[5], o[6], o[7]);
     }
-    if (half == 1u) vbound = fmaxf(vbound, bf16x8_absmax(rv));
-    st_shared_v4(xb + 7 * kAtomBytes + sw128_offset(er, kr), rv.x, rv.y, rv.z, rv.w);
-    return vbound;
+    return bound ? vbound : 0.f;
 }
 
+// Per tile g: both raw tiles, then the peer set of each (once QK(g-1) has
+// read the peer buffer), then the own set of each (once PV(g-2) has read the
+// own stage); a raw stage is released after its own set.
 __device__ void dequant_role(const Ctx& c, const UnitDesc* units, int n_units, int dw) {
     const int lane = threadIdx.x & 31;
-    const int dtid = dw * 32 + lane;
+    const int own_set = (int)c.half, peer_set = 1 - (int)c.half;
     uint32_t g = 0;
     for (int ui = 0; ui < n_units; ++ui) {
         const int n = units[ui].t_end - units[ui].t_begin;
         for (int i = 0; i < n; ++i, ++g) {
-            const uint32_t rs = g % kNR, rph = (g / kNR) & 1u;
-            const uint32_t xs = g % kNX, xph = (g / kNX) & 1u;
-            if (!wait_bar_warp(c, bar_addr(c, BAR_RAW_FULL + rs), rph)) return;
-            if (!wait_bar_warp(c, bar_addr(c, BAR_X_EMPTY + xs), xph ^ 1u)) return;
-            const uint32_t mask = ld_shared_u32(c.sb + kOffRawMask + rs * 4);
-            float vbound = dequant_tile(c.sb + kOffRaw + rs * kRawStageBytes, c.sb + kOffRawSc + rs * kBK * 8,
-                                        c.sb + kOffX + xs * kXStageBytes, mask, dw, lane, c.half);
-            if (dtid == 0) st_shared_u32(c.sb + kOffXMask + xs * 4, mask);
+            uint32_t rs[kRawPerTile], mask[kRawPerTile];
+#pragma unroll
+            for (int k = 0; k < kRawPerTile; ++k) {
+                const uint32_t q = kRawPerTile * g + k;
+                rs[k] = q % kNR;
+                if (!wait_bar_warp(c, bar_addr(c, BAR_RAW_FULL + rs[k]), (q / kNR) & 1u)) return;
+                mask[k] = ld_shared_u32(c.sb + kOffRawMask + rs[k] * 4);
+            }
+            if (!wait_bar_warp(c, bar_addr(c, BAR_XP_EMPTY), (g & 1u) ^ 1u)) return;
+#pragma unroll 1
+            for (int k = 0; k < kRawPerTile; ++k)
+                dequant_set(c.sb + kOffRaw + rs[k] * kRawStageBytes, c.sb + kOffRawSc + rs[k] * kRawBK * 8,
+                            c.sb + kOffXP, kRawBK * k, mask[k], peer_set, dw, lane, false);
+            const uint32_t xs = g % kNXO;
+            if (!wait_bar_warp(c, bar_addr(c, BAR_XO_EMPTY + xs), ((g / kNXO) & 1u) ^ 1u)) return;
+            float vbound = 0.f;
+#pragma unroll 1
+            for (int k = 0; k < kRawPerTile; ++k) {
+                vbound = fmaxf(vbound, dequant_set(c.sb + kOffRaw + rs[k] * kRawStageBytes,
+                                                   c.sb + kOffRawSc + rs[k] * kRawBK * 8, c.sb + kOffXO + xs * kHalfBytes,
+                                                   kRawBK * k, mask[k], own_set, dw, lane, true));
+                __syncwarp();
+                if (lane == 0) mbar_arrive_local(bar_addr(c, BAR_RAW_EMPTY + rs[k]));
+            }
+            if (dw == 0 && lane < kRawPerTile)
+                st_shared_u32(c.sb + kOffXMask + (xs * kRawPerTile + lane) * 4, lane == 0 ? mask[0] : mask[1]);
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) vbound = fmaxf(vbound, __shfl_xor_sync(0xffffffffu, vbound, o));
             if (lane == 0) st_shared_f32(c.sb + kOffXVmax + (xs * kNumDequantWarps + dw) * 4, vbound);
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive_local(bar_addr(c, BAR_X_FULL + xs));
-                mbar_arrive_local(bar_addr(c, BAR_RAW_EMPTY + rs));
-            }
+            if (lane == 0) mbar_arrive_local(bar_addr(c, BAR_X_FULL + xs));
         }
     }
 }
@@ -481,34 +586,37 @@ __device__ void dequant_role(const Ctx& c, const UnitDesc* units, int n_units, i
 // PV(j): O += P(j) . X(j) over this CTA's dims, P as the hi then (unless every
 // softmax warp voted to skip it) the lo bf16 half, both from TMEM.
 __device__ __forceinline__ bool issue_pv(const Ctx& c, uint32_t j, bool first_of_unit) {
-    const uint32_t sb = j & 1u, xs = j % kNX;
+    const uint32_t sb = j & 1u, xs = j % kNXO;
     if (!wait_bar(c, bar_addr(c, BAR_P_FULL + sb), (j >> 1) & 1u)) return false;
     tc_fence_after();
     const uint32_t idesc_pv = idesc_bf16_f32(128, 256, false, true);
-    const uint32_t xb = c.sb + kOffX + xs * kXStageBytes + c.half * 4 * kAtomBytes;
+    const uint64_t bd0 = sdesc_sw128(c.sb + kOffXO + xs * kHalfBytes, kAtomBytes, 1024);
     const uint32_t tp = c.tmem + kTmemS + sb * kBK;
 #pragma unroll
-    for (int kk = 0; kk < kBK / 16; ++kk) {
-        const uint64_t bd = sdesc_sw128(xb + kk * 2048, kAtomBytes, 1024);
-        mma_bf16_ts(c.tmem + kTmemO, tp + kk * 8, bd, idesc_pv, (first_of_unit && kk == 0) ? 0u : 1u);
-    }
+    for (int kk = 0; kk < kBK / 16; ++kk)  // 16 entries (rows) per step: 2048 B
+        mma_bf16_ts(c.tmem + kTmemO, tp + kk * 8, bd0 + (uint64_t)(kk * 2048 >> 4), idesc_pv,
+                    (first_of_unit && kk == 0) ? 0u : 1u);
     uint32_t votes = 1u;
 #pragma unroll
     for (int w = 0; w < kSoftmaxWarps; ++w) votes &= ld_shared_u32(c.sb + kOffVote + (sb * 4 + w) * 4);
     if (votes == 0u) {  // some head needs the lo half of P on this tile
 #pragma unroll
-        for (int kk = 0; kk < kBK / 16; ++kk) {
-            const uint64_t bd = sdesc_sw128(xb + kk * 2048, kAtomBytes, 1024);
-            mma_bf16_ts(c.tmem + kTmemO, tp + kBK / 2 + kk * 8, bd, idesc_pv, 1u);
-        }
+        for (int kk = 0; kk < kBK / 16; ++kk)
+            mma_bf16_ts(c.tmem + kTmemO, tp + kBK / 2 + kk * 8, bd0 + (uint64_t)(kk * 2048 >> 4), idesc_pv, 1u);
     }
-    mma_commit(bar_addr(c, BAR_X_EMPTY + xs));
+    mma_commit(bar_addr(c, BAR_XO_EMPTY + xs));
     mma_commit(bar_addr(c, BAR_O_DONE));
     return true;
 }
 
+// QK(g) then PV(g-1): the tensor pipe runs QK(g) while the softmax works on
+// tile g-1.  K = 512 in 32 steps of 16 dims: dims 0..255 with Q from TMEM,
+// 256..511 with Q from shared memory; the B operand of a step comes from the
+// own or the peer buffer, whichever holds its dims.
 __device__ void mma_role(const Ctx& c, const UnitDesc* units, int n_units) {
     const uint32_t idesc_qk = idesc_bf16_f32(128, kBK, false, false);
+    const uint64_t q_desc0 = sdesc_sw128(c.sb + kOffQ, 16, 1024);
+    const uint64_t xp_desc0 = sdesc_sw128(c.sb + kOffXP, 16, 1024);
     uint32_t g = 0;
     bool ok = true;
     for (int ui = 0; ui < n_units && ok; ++ui) {
@@ -517,24 +625,27 @@ __device__ void mma_role(const Ctx& c, const UnitDesc* units, int n_units) {
         tc_fence_after();
         const uint32_t g0 = g;
         for (int i = 0; i < n; ++i, ++g) {
-            const uint32_t xs = g % kNX;
-            if (!wait_bar(c, bar_addr(c, BAR_X_FULL + xs), (g / kNX) & 1u)) { ok = false; break; }
+            const uint32_t xs = g % kNXO;
+            if (!wait_bar(c, bar_addr(c, BAR_X_FULL + xs), (g / kNXO) & 1u)) { ok = false; break; }
             tc_fence_after();
-            const uint32_t xb = c.sb + kOffX + xs * kXStageBytes;
+            const uint64_t xo_desc0 = sdesc_sw128(c.sb + kOffXO + xs * kHalfBytes, 16, 1024);
+            // dims [256 h, 256 h + 256) are in the own buffer, the rest in the peer buffer
+            const uint64_t lo_desc = c.half == 0 ? xo_desc0 : xp_desc0;  // dims 0..255
+            const uint64_t hi_desc = c.half == 0 ? xp_desc0 : xo_desc0;  // dims 256..511
             const uint32_t ts = c.tmem + kTmemS + (g & 1u) * kBK;
-            // K = 512 in 32 steps: dims 0..255 with Q from TMEM, 256..511 with Q from shared memory
 #pragma unroll
             for (int kk = 0; kk < 16; ++kk) {
-                const uint64_t bd = sdesc_sw128(xb + (kk >> 2) * kAtomBytes + (kk & 3) * 32, 16, 1024);
+                const uint64_t bd = lo_desc + (uint64_t)(((kk >> 2) * kAtomBytes + (kk & 3) * 32) >> 4);
                 mma_bf16_ts(ts, c.tmem + kTmemQ + kk * 8, bd, idesc_qk, kk > 0 ? 1u : 0u);
             }
 #pragma unroll
-            for (int kk = 16; kk < 32; ++kk) {
-                const uint64_t ad = sdesc_sw128(c.sb + kOffQ + ((kk - 16) >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-                const uint64_t bd = sdesc_sw128(xb + (kk >> 2) * kAtomBytes + (kk & 3) * 32, 16, 1024);
+            for (int kk = 0; kk < 16; ++kk) {
+                const uint64_t ad = q_desc0 + (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+                const uint64_t bd = hi_desc + (uint64_t)(((kk >> 2) * kAtomBytes + (kk & 3) * 32) >> 4);
                 mma_bf16_ss(ts, ad, bd, idesc_qk, 1u);
             }
             mma_commit(bar_addr(c, BAR_S_FULL + (g & 1u)));
+            mma_commit(bar_addr(c, BAR_XP_EMPTY));
             if (i > 0 && !issue_pv(c, g - 1, (g - 1) == g0)) { ok = false; break; }
         }
         if (ok && n > 0 && !issue_pv(c, g - 1, (g - 1) == g0)) ok = false;
@@ -606,16 +717,22 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, const UnitDesc* uni
             // The tile's valid mask and |V| bound were written before its X_FULL
             // arrival; X_FULL of this tile cannot have advanced further (its stage
             // is refilled only after PV of this tile, which needs this thread's P).
-            if (!wait_bar_warp(c, bar_addr(c, BAR_X_FULL + g % kNX), (g / kNX) & 1u)) { ok = false; break; }
+            if (!wait_bar_warp(c, bar_addr(c, BAR_X_FULL + g % kNXO), (g / kNXO) & 1u)) { ok = false; break; }
             tc_fence_after();
-            const uint32_t vmask = ld_shared_u32(c.sb + kOffXMask + (g % kNX) * 4);
+            const uint32_t xs = g % kNXO;
+            const uint32_t vmask0 = ld_shared_u32(c.sb + kOffXMask + (xs * kRawPerTile) * 4);
+            const uint32_t vmask1 = ld_shared_u32(c.sb + kOffXMask + (xs * kRawPerTile + 1) * 4);
             float s[kBK];
             {
                 uint32_t v[32];
                 tmem_ld32(ts, v);
                 tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < kBK; ++j) s[j] = ((vmask >> j) & 1u) ? __uint_as_float(v[j]) * qscale : -INFINITY;
+                for (int j = 0; j < 32; ++j) s[j] = ((vmask0 >> j) & 1u) ? __uint_as_float(v[j]) * qscale : -INFINITY;
+                tmem_ld32(ts + 32, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) s[32 + j] = ((vmask1 >> j) & 1u) ? __uint_as_float(v[j]) * qscale : -INFINITY;
             }
             float mx[8];
 #pragma unroll
@@ -630,25 +747,28 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, const UnitDesc* uni
             const bool rescale = o_init && (m_new != m_used);
             m_used = m_new;
             // ---- P = 2^(s - m) as a bf16 hi/lo pair, written back over the scores
-            // (hi in columns [0, 16), lo in [16, 32)).  Safe before PV(g-1) completes:
+            // (hi in columns [0, 32), lo in [32, 64)).  Safe before PV(g-1) completes:
             // these columns were last read by PV(g-2), which retired before QK(g)
             // (same issue stream) produced this tile's scores.
             float ps = 0.f, lo_abs = 0.f;
             {
-                uint32_t hv[16], lv[16];
                 float sm[4] = {0.f, 0.f, 0.f, 0.f}, la[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const float p0 = ex2_approx(s[2 * j] - msub), p1 = ex2_approx(s[2 * j + 1] - msub);
-                    sm[j & 3] += p0 + p1;
-                    split_bf16x2(p0, p1, hv[j], lv[j]);
-                    const __nv_bfloat162 lb = *reinterpret_cast<const __nv_bfloat162*>(&lv[j]);
-                    la[j & 3] += fabsf(__low2float(lb)) + fabsf(__high2float(lb));
+                for (int hf = 0; hf < 2; ++hf) {  // entries 32 hf .. 32 hf + 31
+                    uint32_t hv[16], lv[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float p0 = ex2_approx(s[32 * hf + 2 * j] - msub), p1 = ex2_approx(s[32 * hf + 2 * j + 1] - msub);
+                        sm[j & 3] += p0 + p1;
+                        split_bf16x2(p0, p1, hv[j], lv[j]);
+                        const __nv_bfloat162 lb = *reinterpret_cast<const __nv_bfloat162*>(&lv[j]);
+                        la[j & 3] += fabsf(__low2float(lb)) + fabsf(__high2float(lb));
+                    }
+                    tmem_st16(ts + 16 * hf, hv);
+                    tmem_st16(ts + kBK / 2 + 16 * hf, lv);
                 }
                 ps = (sm[0] + sm[1]) + (sm[2] + sm[3]);
                 lo_abs = (la[0] + la[1]) + (la[2] + la[3]);
-                tmem_st16(ts, hv);
-                tmem_st16(ts + kBK / 2, lv);
             }
             lsum = lsum * alpha + ps;
             skipped *= alpha;
@@ -673,7 +793,7 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, const UnitDesc* uni
             }
             // vote on skipping the lo half: sum|lo| x max|V| (this CTA's dims) bounds what skipping drops
             {
-                const uint32_t vb = c.sb + kOffXVmax + (g % kNX) * (4 * kNumDequantWarps);
+                const uint32_t vb = c.sb + kOffXVmax + xs * (4 * kNumDequantWarps);
                 float vmax = ld_shared_f32(vb);
 #pragma unroll
                 for (int w = 1; w < kNumDequantWarps; ++w) vmax = fmaxf(vmax, ld_shared_f32(vb + 4 * w));
@@ -851,10 +971,11 @@ __global__ void __launch_bounds__(kThreads, 1) smla_decode_kernel(const KParams 
             mbar_init(bar_addr(c, BAR_RAW_FULL + i), 33);  // 32 async (cp.async) + 1 (producer lane 0)
             mbar_init(bar_addr(c, BAR_RAW_EMPTY + i), kNumDequantWarps);
         }
-        for (int i = 0; i < kNX; ++i) {
+        for (int i = 0; i < kNXO; ++i) {
             mbar_init(bar_addr(c, BAR_X_FULL + i), kNumDequantWarps);
-            mbar_init(bar_addr(c, BAR_X_EMPTY + i), 1);
+            mbar_init(bar_addr(c, BAR_XO_EMPTY + i), 1);
         }
+        mbar_init(bar_addr(c, BAR_XP_EMPTY), 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar_addr(c, BAR_S_FULL + i), 1);
             mbar_init(bar_addr(c, BAR_P_FULL + i), kSoftmaxWarps);

@@ -251,3 +251,55 @@ def test_ragged_long_context_all_rows(cuda_device):
     out, lse = run_gpu(p, num_splits=S)
     ro, rl = run_oracle(p)
     assert_close(out, lse, ro, rl, what="ragged")
+
+
+def _referenced_main_entries(p, row):
+    """Physical main-pool rows that `row` reads through its top-k slots."""
+    idx = [v for v in p.main_idx[row].tolist() if v != -1]
+    bt = p.block_table
+    seq = int(p.row_seq[row]) if p.row_seq is not None else row
+    out = []
+    for pos in idx:
+        if bt is None:
+            out.append(pos)
+        else:
+            out.append(int(bt[seq, pos // 64]) * 64 + pos % 64)
+    return sorted(set(out))
+
+
+def test_scale_codes_outside_the_fast_range(cuda_device):
+    # Scale codes 0..9 and 135..254 are converted by the exact path; the
+    # bytes under the large codes are kept to small subnormal e4m3 values so
+    # that the scores stay in a range where fp32 accumulation is accurate.
+    p = small(H=64, seq_lens=(3000, 2000), topk=256, swa=64, invalid=0.05, seed=21)
+    ents = _referenced_main_entries(p, 0)
+    g = torch.Generator().manual_seed(5)
+    pick = torch.tensor(ents, dtype=torch.long)[torch.randperm(len(ents), generator=g)[:48]].cuda()
+    big, tiny_ = pick[:24], pick[24:]
+    grp = 3  # dims 192..255
+    small_bytes = torch.randint(0, 8, (big.numel(), 64), generator=g, dtype=torch.uint8)
+    small_bytes |= (torch.randint(0, 2, small_bytes.shape, generator=g, dtype=torch.uint8) << 7)
+    p.kv_pool[big, 64 * grp:64 * grp + 64] = small_bytes.cuda()
+    p.kv_scales[big, grp] = 140
+    p.kv_scales[tiny_, 1] = 4
+    p.kv_scales[tiny_, 5] = 0
+    check(p, num_splits=1, what="codes s1")
+    check(p, num_splits=3, what="codes s3")
+
+
+@pytest.mark.parametrize("dim", [10, 300])
+def test_nan_byte_in_a_selected_entry_propagates(cuda_device, dim):
+    # e4m3 0x7F is NaN: every row that reads the entry gets NaN, as in the
+    # oracle; rows that do not read it stay finite and close.
+    p = small(H=32, seq_lens=(2000, 1500), topk=128, swa=64, invalid=0.05, seed=22)
+    e = _referenced_main_entries(p, 0)[3]
+    p.kv_pool[e, dim] = 0x7F
+    out, lse = run_gpu(p, num_splits=2)
+    ro, rl = run_oracle(p)
+    o = out.float().cpu().numpy().astype(np.float64)
+    l = lse.float().cpu().numpy().astype(np.float64)
+    assert np.isnan(ro[0]).all() and np.isnan(rl[0]).all()
+    assert np.array_equal(np.isnan(o), np.isnan(ro)), "NaN pattern differs from the oracle"
+    assert np.array_equal(np.isnan(l), np.isnan(rl))
+    fin = ~np.isnan(ro)
+    assert (np.abs(o[fin] - ro[fin]) <= 1e-2 + 1e-2 * np.abs(ro[fin])).all()
