@@ -123,8 +123,9 @@ static_assert(4 * (2 * SMLA_MAX_ROWS + 8) <= kNR * kRawStageBytes, "plan scratch
 enum : uint32_t {
     BAR_RAW_FULL = 0,                      // [kNR] producer -> dequant (32 async + 1 arrival, tx bytes)
     BAR_RAW_EMPTY = BAR_RAW_FULL + kNR,    // [kNR] dequant -> producer (kNumDequantWarps)
-    BAR_X_FULL = BAR_RAW_EMPTY + kNR,      // [kNXO] dequant -> MMA, softmax (kNumDequantWarps)
-    BAR_XO_EMPTY = BAR_X_FULL + kNXO,      // [kNXO] MMA commit after PV (own dims free)
+    BAR_X_FULL = BAR_RAW_EMPTY + kNR,      // [kNXO] own dims written: dequant -> MMA, softmax (kNumDequantWarps)
+    BAR_XP_FULL = BAR_X_FULL + kNXO,       // peer dims written: dequant -> MMA (kNumDequantWarps)
+    BAR_XO_EMPTY = BAR_XP_FULL + 1,        // [kNXO] MMA commit after PV (own dims free)
     BAR_XP_EMPTY = BAR_XO_EMPTY + kNXO,    // MMA commit after QK (peer dims free)
     BAR_S_FULL = BAR_XP_EMPTY + 1,         // [2] MMA commit after QK
     BAR_P_FULL = BAR_S_FULL + 2,           // [2] softmax -> MMA (kSoftmaxWarps)
@@ -428,14 +429,31 @@ __device__ void producer_role(const KParams& p, const Ctx& c, const UnitDesc* un
                 sp = static_cast<const uint8_t*>(cmp ? a.cmp_scales : a.kv_scales) + phys * SMLA_SCALE_BYTES;
             }
             const uint32_t mask = __ballot_sync(0xffffffffu, ep != nullptr);
+            // A run of consecutive pool rows in lanes 0..n-1 (compressed entries,
+            // window entries within a page) moves as one bulk copy; other tiles
+            // take one copy per entry.
+            const uint8_t* ep0 = reinterpret_cast<const uint8_t*>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(ep), 0));
+            const int nvalid = __popc(mask);
+            const bool run = (mask == (nvalid == 32 ? 0xffffffffu : (1u << nvalid) - 1u)) &&
+                             __all_sync(0xffffffffu, ep == nullptr || ep == ep0 + (size_t)lane * SMLA_ENTRY_BYTES);
+            // Start the entries' trip from HBM now; the copy into the stage, once
+            // the stage is free, then finds them in L2.
+            if (run) {
+                if (lane == 0 && nvalid > 0) bulk_prefetch_l2(ep0, (uint32_t)nvalid * SMLA_ENTRY_BYTES);
+            } else if (ep != nullptr) {
+                bulk_prefetch_l2(ep, SMLA_ENTRY_BYTES);
+            }
             if (!wait_bar_warp(c, bar_addr(c, BAR_RAW_EMPTY + rs), rph ^ 1u)) return;
             const uint32_t full = bar_addr(c, BAR_RAW_FULL + rs);
-            if (lane == 0) mbar_expect_tx_only(full, (uint32_t)__popc(mask) * SMLA_ENTRY_BYTES);
+            if (lane == 0) mbar_expect_tx_only(full, (uint32_t)nvalid * SMLA_ENTRY_BYTES);
             __syncwarp();
-            if (ep != nullptr) {
-                bulk_g2s(c.sb + kOffRaw + rs * kRawStageBytes + lane * SMLA_ENTRY_BYTES, ep, SMLA_ENTRY_BYTES, full);
-                cp_async_8(c.sb + kOffRawSc + (rs * kRawBK + lane) * 8, sp);
+            const uint32_t dst = c.sb + kOffRaw + rs * kRawStageBytes;
+            if (run) {
+                if (lane == 0 && nvalid > 0) bulk_g2s(dst, ep0, (uint32_t)nvalid * SMLA_ENTRY_BYTES, full);
+            } else if (ep != nullptr) {
+                bulk_g2s(dst + lane * SMLA_ENTRY_BYTES, ep, SMLA_ENTRY_BYTES, full);
             }
+            if (ep != nullptr) cp_async_8(c.sb + kOffRawSc + (rs * kRawBK + lane) * 8, sp);
             cp_async_arrive_noinc(full);  // one of the 32 async arrivals
             if (lane == 0) {
                 st_shared_u32(c.sb + kOffRawMask + rs * 4, mask);
@@ -534,9 +552,10 @@ __device__ __forceinline__ float dequant_set(uint32_t raw, uint32_t rawsc, uint3
     return bound ? vbound : 0.f;
 }
 
-// Per tile g: both raw tiles, then the peer set of each (once QK(g-1) has
-// read the peer buffer), then the own set of each (once PV(g-2) has read the
-// own stage); a raw stage is released after its own set.
+// Per tile g: the peer set of both raw tiles (once QK(g-1) has read the peer
+// buffer), announced on XP_FULL so that QK(g) can start on those dims; then
+// the own set of both (once PV(g-2) has read the own stage), releasing each
+// raw stage after it, announced on X_FULL.
 __device__ void dequant_role(const Ctx& c, const UnitDesc* units, int n_units, int dw) {
     const int lane = threadIdx.x & 31;
     const int own_set = (int)c.half, peer_set = 1 - (int)c.half;
@@ -544,23 +563,24 @@ __device__ void dequant_role(const Ctx& c, const UnitDesc* units, int n_units, i
     for (int ui = 0; ui < n_units; ++ui) {
         const int n = units[ui].t_end - units[ui].t_begin;
         for (int i = 0; i < n; ++i, ++g) {
-            uint32_t rs[kRawPerTile], mask[kRawPerTile];
+            const uint32_t xs = g % kNXO;
+            uint32_t mask[kRawPerTile], rs[kRawPerTile];
 #pragma unroll
             for (int k = 0; k < kRawPerTile; ++k) {
                 const uint32_t q = kRawPerTile * g + k;
                 rs[k] = q % kNR;
                 if (!wait_bar_warp(c, bar_addr(c, BAR_RAW_FULL + rs[k]), (q / kNR) & 1u)) return;
                 mask[k] = ld_shared_u32(c.sb + kOffRawMask + rs[k] * 4);
-            }
-            if (!wait_bar_warp(c, bar_addr(c, BAR_XP_EMPTY), (g & 1u) ^ 1u)) return;
-#pragma unroll 1
-            for (int k = 0; k < kRawPerTile; ++k)
+                if (k == 0 && !wait_bar_warp(c, bar_addr(c, BAR_XP_EMPTY), (g & 1u) ^ 1u)) return;
                 dequant_set(c.sb + kOffRaw + rs[k] * kRawStageBytes, c.sb + kOffRawSc + rs[k] * kRawBK * 8,
                             c.sb + kOffXP, kRawBK * k, mask[k], peer_set, dw, lane, false);
-            const uint32_t xs = g % kNXO;
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_local(bar_addr(c, BAR_XP_FULL));
             if (!wait_bar_warp(c, bar_addr(c, BAR_XO_EMPTY + xs), ((g / kNXO) & 1u) ^ 1u)) return;
             float vbound = 0.f;
-#pragma unroll 1
+#pragma unroll
             for (int k = 0; k < kRawPerTile; ++k) {
                 vbound = fmaxf(vbound, dequant_set(c.sb + kOffRaw + rs[k] * kRawStageBytes,
                                                    c.sb + kOffRawSc + rs[k] * kRawBK * 8, c.sb + kOffXO + xs * kHalfBytes,
@@ -592,9 +612,10 @@ __device__ __forceinline__ bool issue_pv(const Ctx& c, uint32_t j, bool first_of
     const uint32_t idesc_pv = idesc_bf16_f32(128, 256, false, true);
     const uint64_t bd0 = sdesc_sw128(c.sb + kOffXO + xs * kHalfBytes, kAtomBytes, 1024);
     const uint32_t tp = c.tmem + kTmemS + sb * kBK;
+    // P of entries 16 kk .. 16 kk + 15: hi at columns [16 kk, 16 kk + 8), lo in the next 8
 #pragma unroll
     for (int kk = 0; kk < kBK / 16; ++kk)  // 16 entries (rows) per step: 2048 B
-        mma_bf16_ts(c.tmem + kTmemO, tp + kk * 8, bd0 + (uint64_t)(kk * 2048 >> 4), idesc_pv,
+        mma_bf16_ts(c.tmem + kTmemO, tp + 16 * kk, bd0 + (uint64_t)(kk * 2048 >> 4), idesc_pv,
                     (first_of_unit && kk == 0) ? 0u : 1u);
     uint32_t votes = 1u;
 #pragma unroll
@@ -602,7 +623,7 @@ __device__ __forceinline__ bool issue_pv(const Ctx& c, uint32_t j, bool first_of
     if (votes == 0u) {  // some head needs the lo half of P on this tile
 #pragma unroll
         for (int kk = 0; kk < kBK / 16; ++kk)
-            mma_bf16_ts(c.tmem + kTmemO, tp + kBK / 2 + kk * 8, bd0 + (uint64_t)(kk * 2048 >> 4), idesc_pv, 1u);
+            mma_bf16_ts(c.tmem + kTmemO, tp + 16 * kk + 8, bd0 + (uint64_t)(kk * 2048 >> 4), idesc_pv, 1u);
     }
     mma_commit(bar_addr(c, BAR_XO_EMPTY + xs));
     mma_commit(bar_addr(c, BAR_O_DONE));
@@ -626,27 +647,51 @@ __device__ void mma_role(const Ctx& c, const UnitDesc* units, int n_units) {
         const uint32_t g0 = g;
         for (int i = 0; i < n; ++i, ++g) {
             const uint32_t xs = g % kNXO;
-            if (!wait_bar(c, bar_addr(c, BAR_X_FULL + xs), (g / kNXO) & 1u)) { ok = false; break; }
+            if (!wait_bar(c, bar_addr(c, BAR_XP_FULL), g & 1u)) { ok = false; break; }
             tc_fence_after();
             const uint64_t xo_desc0 = sdesc_sw128(c.sb + kOffXO + xs * kHalfBytes, 16, 1024);
             // dims [256 h, 256 h + 256) are in the own buffer, the rest in the peer buffer
             const uint64_t lo_desc = c.half == 0 ? xo_desc0 : xp_desc0;  // dims 0..255
             const uint64_t hi_desc = c.half == 0 ? xp_desc0 : xo_desc0;  // dims 256..511
             const uint32_t ts = c.tmem + kTmemS + (g & 1u) * kBK;
+            bool pv_issued = false;
+            // The peer dims' K steps go first (the dequant writes them first) and
+            // their completion frees the peer buffer, so the dequant of the next
+            // tile's peer dims overlaps the own dims' K steps.
 #pragma unroll
-            for (int kk = 0; kk < 16; ++kk) {
-                const uint64_t bd = lo_desc + (uint64_t)(((kk >> 2) * kAtomBytes + (kk & 3) * 32) >> 4);
-                mma_bf16_ts(ts, c.tmem + kTmemQ + kk * 8, bd, idesc_qk, kk > 0 ? 1u : 0u);
-            }
+            for (int part = 0; part < 2; ++part) {
+                if (part == 1) {
+                    if (!wait_bar(c, bar_addr(c, BAR_X_FULL + xs), (g / kNXO) & 1u)) { ok = false; break; }
+                    tc_fence_after();
+                }
+                const bool lo_dims = (part == 0) == (c.half == 1);  // dims 0..255 are peer dims for half 1
+                if (lo_dims) {
 #pragma unroll
-            for (int kk = 0; kk < 16; ++kk) {
-                const uint64_t ad = q_desc0 + (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-                const uint64_t bd = hi_desc + (uint64_t)(((kk >> 2) * kAtomBytes + (kk & 3) * 32) >> 4);
-                mma_bf16_ss(ts, ad, bd, idesc_qk, 1u);
+                    for (int kk = 0; kk < 16; ++kk) {
+                        const uint64_t bd = lo_desc + (uint64_t)(((kk >> 2) * kAtomBytes + (kk & 3) * 32) >> 4);
+                        mma_bf16_ts(ts, c.tmem + kTmemQ + kk * 8, bd, idesc_qk, (part == 0 && kk == 0) ? 0u : 1u);
+                    }
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < 16; ++kk) {
+                        const uint64_t ad = q_desc0 + (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+                        const uint64_t bd = hi_desc + (uint64_t)(((kk >> 2) * kAtomBytes + (kk & 3) * 32) >> 4);
+                        mma_bf16_ss(ts, ad, bd, idesc_qk, (part == 0 && kk == 0) ? 0u : 1u);
+                    }
+                }
+                if (part == 0) {
+                    mma_commit(bar_addr(c, BAR_XP_EMPTY));
+                    // PV(g-1) goes between the halves when its P is already
+                    // there: it then frees the own stage of tile g+1 earlier.
+                    if (i > 0 && mbar_test_wait(bar_addr(c, BAR_P_FULL + ((g - 1) & 1u)), ((g - 1) >> 1) & 1u)) {
+                        if (!issue_pv(c, g - 1, (g - 1) == g0)) { ok = false; break; }
+                        pv_issued = true;
+                    }
+                }
             }
+            if (!ok) break;
             mma_commit(bar_addr(c, BAR_S_FULL + (g & 1u)));
-            mma_commit(bar_addr(c, BAR_XP_EMPTY));
-            if (i > 0 && !issue_pv(c, g - 1, (g - 1) == g0)) { ok = false; break; }
+            if (i > 0 && !pv_issued && !issue_pv(c, g - 1, (g - 1) == g0)) { ok = false; break; }
         }
         if (ok && n > 0 && !issue_pv(c, g - 1, (g - 1) == g0)) ok = false;
     }
@@ -722,23 +767,21 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, const UnitDesc* uni
             const uint32_t xs = g % kNXO;
             const uint32_t vmask0 = ld_shared_u32(c.sb + kOffXMask + (xs * kRawPerTile) * 4);
             const uint32_t vmask1 = ld_shared_u32(c.sb + kOffXMask + (xs * kRawPerTile + 1) * 4);
-            float s[kBK];
-            {
+            // pass 1: the tile's masked maximum (scores are reloaded in pass 2, so
+            // only 32 of them are live at a time)
+            float mt = -INFINITY;
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
                 uint32_t v[32];
-                tmem_ld32(ts, v);
+                tmem_ld32(ts + 32 * hf, v);
                 tmem_wait_ld();
+                const uint32_t vm = hf == 0 ? vmask0 : vmask1;
+                float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                for (int j = 0; j < 32; ++j) s[j] = ((vmask0 >> j) & 1u) ? __uint_as_float(v[j]) * qscale : -INFINITY;
-                tmem_ld32(ts + 32, v);
-                tmem_wait_ld();
-#pragma unroll
-                for (int j = 0; j < 32; ++j) s[32 + j] = ((vmask1 >> j) & 1u) ? __uint_as_float(v[j]) * qscale : -INFINITY;
+                for (int j = 0; j < 32; ++j)
+                    mx[j & 3] = fmaxf(mx[j & 3], ((vm >> j) & 1u) ? __uint_as_float(v[j]) * qscale : -INFINITY);
+                mt = fmaxf(mt, fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])));
             }
-            float mx[8];
-#pragma unroll
-            for (int j = 0; j < kBK; ++j) mx[j & 7] = (j < 8) ? s[j] : fmaxf(mx[j & 7], s[j]);
-            const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
             float m_new = m_used;
             if (m_used == -INFINITY || mt > m_used + kRescaleThreshold) m_new = fmaxf(m_used, mt);
             const float alpha = (m_used == -INFINITY) ? 0.f : ex2_approx(m_used - m_new);
@@ -746,29 +789,40 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, const UnitDesc* uni
             const float msub = (m_new == -INFINITY) ? 0.f : m_new;
             const bool rescale = o_init && (m_new != m_used);
             m_used = m_new;
-            // ---- P = 2^(s - m) as a bf16 hi/lo pair, written back over the scores
-            // (hi in columns [0, 32), lo in [32, 64)).  Safe before PV(g-1) completes:
-            // these columns were last read by PV(g-2), which retired before QK(g)
-            // (same issue stream) produced this tile's scores.
+            // ---- pass 2: P = 2^(s - m) as a bf16 pair hi = bf16(p), lo = bf16(p - hi),
+            // written back over the scores one 16-entry step at a time: entries
+            // 16 q .. 16 q + 15 (columns [16 q, 16 q + 16)) become hi in columns
+            // [16 q, 16 q + 8) and lo in [16 q + 8, 16 q + 16).  Safe before PV(g-1)
+            // completes: these columns were last read by PV(g-2), which retired
+            // before QK(g) (same issue stream) produced this tile's scores.
             float ps = 0.f, lo_abs = 0.f;
             {
                 float sm[4] = {0.f, 0.f, 0.f, 0.f}, la[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+                for (int q = 0; q < kBK / 16; ++q) {
+                    uint32_t v[16];
+                    tmem_ld16(ts + 16 * q, v);
+                    tmem_wait_ld();
+                    const uint32_t vm = ((q < 2 ? vmask0 : vmask1) >> (16 * (q & 1))) & 0xFFFFu;
+                    uint32_t hv[8], lv[8];
 #pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {  // entries 32 hf .. 32 hf + 31
-                    uint32_t hv[16], lv[16];
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const float p0 = ex2_approx(s[32 * hf + 2 * j] - msub), p1 = ex2_approx(s[32 * hf + 2 * j + 1] - msub);
+                    for (int j = 0; j < 8; ++j) {
+                        const float x0 = ((vm >> (2 * j)) & 1u) ? fmaf(__uint_as_float(v[2 * j]), qscale, -msub) : -INFINITY;
+                        const float x1 = ((vm >> (2 * j + 1)) & 1u) ? fmaf(__uint_as_float(v[2 * j + 1]), qscale, -msub) : -INFINITY;
+                        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
                         sm[j & 3] += p0 + p1;
-                        split_bf16x2(p0, p1, hv[j], lv[j]);
-                        const __nv_bfloat162 lb = *reinterpret_cast<const __nv_bfloat162*>(&lv[j]);
-                        la[j & 3] += fabsf(__low2float(lb)) + fabsf(__high2float(lb));
+                        const __nv_bfloat162 hb = __floats2bfloat162_rn(p0, p1);
+                        const float r0 = p0 - __low2float(hb), r1 = p1 - __high2float(hb);
+                        memcpy(&hv[j], &hb, 4);
+                        lv[j] = pack_bf16(r0, r1);
+                        la[j & 3] += fabsf(r0) + fabsf(r1);
                     }
-                    tmem_st16(ts + 16 * hf, hv);
-                    tmem_st16(ts + kBK / 2 + 16 * hf, lv);
+                    tmem_st8(ts + 16 * q, hv);
+                    tmem_st8(ts + 16 * q + 8, lv);
                 }
                 ps = (sm[0] + sm[1]) + (sm[2] + sm[3]);
-                lo_abs = (la[0] + la[1]) + (la[2] + la[3]);
+                // |bf16(r)| <= |r| (1 + 2^-8): a bound on the sum of |lo|
+                lo_abs = ((la[0] + la[1]) + (la[2] + la[3])) * (1.0f + 1.0f / 256.0f);
             }
             lsum = lsum * alpha + ps;
             skipped *= alpha;
@@ -976,6 +1030,7 @@ __global__ void __launch_bounds__(kThreads, 1) smla_decode_kernel(const KParams 
             mbar_init(bar_addr(c, BAR_XO_EMPTY + i), 1);
         }
         mbar_init(bar_addr(c, BAR_XP_EMPTY), 1);
+        mbar_init(bar_addr(c, BAR_XP_FULL), kNumDequantWarps);
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar_addr(c, BAR_S_FULL + i), 1);
             mbar_init(bar_addr(c, BAR_P_FULL + i), kSoftmaxWarps);
