@@ -535,16 +535,19 @@ __device__ __forceinline__ float dequant_set(uint32_t raw, uint32_t rawsc, uint3
             st_shared_v4(dst + 3 * kAtomBytes + sw128_offset(row0 + er[it], kr), rv[it].x, rv[it].y, rv[it].z, rv[it].w);
         }
     }
-    if (__any_sync(0xffffffffu, bad[0] || bad[1])) {
-#pragma unroll
+    if (__any_sync(0xffffffffu, bad[0] || bad[1])) {  // rare: one copy of the exact path
+#pragma unroll 1
         for (int it = 0; it < 2; ++it) {
-            if (!bad[it]) continue;
-            const float scale = ue8m0_to_f32(code[it]);
+            const bool b = it == 0 ? bad[0] : bad[1];
+            if (!b) continue;
+            const uint4 vv = it == 0 ? v[0] : v[1];
+            const uint32_t cd = it == 0 ? code[0] : code[1];
+            const float scale = ue8m0_to_f32(cd);
             uint32_t o[8];
-            dequant16(v[it], scale, o);
-            const float bnd = e4m3x16_absmax(v[it]) * scale;
+            dequant16(vv, scale, o);
+            const float bnd = e4m3x16_absmax(vv) * scale;
             vbound = (bnd > vbound || bnd != bnd) ? (bnd != bnd ? INFINITY : bnd) : vbound;
-            const uint32_t d = dst + (atom[it] & 3) * kAtomBytes;
+            const uint32_t d = dst + ((it == 0 ? atom[0] : atom[1]) & 3) * kAtomBytes;
             st_shared_v4(d + sw128_offset(row0 + ef, kk), o[0], o[1], o[2], o[3]);
             st_shared_v4(d + sw128_offset(row0 + ef, kk + 1), o[4], o[5], o[6], o[7]);
         }
@@ -552,44 +555,48 @@ __device__ __forceinline__ float dequant_set(uint32_t raw, uint32_t rawsc, uint3
     return bound ? vbound : 0.f;
 }
 
-// Per tile g: the peer set of both raw tiles (once QK(g-1) has read the peer
-// buffer), announced on XP_FULL so that QK(g) can start on those dims; then
-// the own set of both (once PV(g-2) has read the own stage), releasing each
-// raw stage after it, announced on X_FULL.
+// Per tile g, four steps with one call site (the role's code stays small in
+// the instruction cache): the peer set of raw tile 0 and 1 (once QK(g-1) has
+// read the peer buffer), announced on XP_FULL so that QK(g) can start on those
+// dims; then the own set of raw tile 0 and 1 (once PV(g-2) has read the own
+// stage), each raw stage released after its own set; announced on X_FULL.
 __device__ void dequant_role(const Ctx& c, const UnitDesc* units, int n_units, int dw) {
     const int lane = threadIdx.x & 31;
-    const int own_set = (int)c.half, peer_set = 1 - (int)c.half;
     uint32_t g = 0;
     for (int ui = 0; ui < n_units; ++ui) {
         const int n = units[ui].t_end - units[ui].t_begin;
         for (int i = 0; i < n; ++i, ++g) {
             const uint32_t xs = g % kNXO;
-            uint32_t mask[kRawPerTile], rs[kRawPerTile];
-#pragma unroll
-            for (int k = 0; k < kRawPerTile; ++k) {
-                const uint32_t q = kRawPerTile * g + k;
-                rs[k] = q % kNR;
-                if (!wait_bar_warp(c, bar_addr(c, BAR_RAW_FULL + rs[k]), (q / kNR) & 1u)) return;
-                mask[k] = ld_shared_u32(c.sb + kOffRawMask + rs[k] * 4);
-                if (k == 0 && !wait_bar_warp(c, bar_addr(c, BAR_XP_EMPTY), (g & 1u) ^ 1u)) return;
-                dequant_set(c.sb + kOffRaw + rs[k] * kRawStageBytes, c.sb + kOffRawSc + rs[k] * kRawBK * 8,
-                            c.sb + kOffXP, kRawBK * k, mask[k], peer_set, dw, lane, false);
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_local(bar_addr(c, BAR_XP_FULL));
-            if (!wait_bar_warp(c, bar_addr(c, BAR_XO_EMPTY + xs), ((g / kNXO) & 1u) ^ 1u)) return;
+            uint32_t mask0 = 0u, mask1 = 0u;
             float vbound = 0.f;
-#pragma unroll
-            for (int k = 0; k < kRawPerTile; ++k) {
-                vbound = fmaxf(vbound, dequant_set(c.sb + kOffRaw + rs[k] * kRawStageBytes,
-                                                   c.sb + kOffRawSc + rs[k] * kRawBK * 8, c.sb + kOffXO + xs * kHalfBytes,
-                                                   kRawBK * k, mask[k], own_set, dw, lane, true));
-                __syncwarp();
-                if (lane == 0) mbar_arrive_local(bar_addr(c, BAR_RAW_EMPTY + rs[k]));
+#pragma unroll 1
+            for (int step = 0; step < 2 * kRawPerTile; ++step) {
+                const int k = step & 1;
+                const bool own = step >= kRawPerTile;
+                const uint32_t q = kRawPerTile * g + k;
+                const uint32_t rs = q % kNR;
+                if (!own) {
+                    if (!wait_bar_warp(c, bar_addr(c, BAR_RAW_FULL + rs), (q / kNR) & 1u)) return;
+                    const uint32_t m = ld_shared_u32(c.sb + kOffRawMask + rs * 4);
+                    if (k == 0) mask0 = m; else mask1 = m;
+                    if (k == 0 && !wait_bar_warp(c, bar_addr(c, BAR_XP_EMPTY), (g & 1u) ^ 1u)) return;
+                } else if (k == 0) {
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_local(bar_addr(c, BAR_XP_FULL));
+                    if (!wait_bar_warp(c, bar_addr(c, BAR_XO_EMPTY + xs), ((g / kNXO) & 1u) ^ 1u)) return;
+                }
+                const uint32_t dst = own ? c.sb + kOffXO + xs * kHalfBytes : c.sb + kOffXP;
+                const int set = own ? (int)c.half : 1 - (int)c.half;
+                vbound = fmaxf(vbound, dequant_set(c.sb + kOffRaw + rs * kRawStageBytes, c.sb + kOffRawSc + rs * kRawBK * 8,
+                                                   dst, kRawBK * k, k == 0 ? mask0 : mask1, set, dw, lane, own));
+                if (own) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_local(bar_addr(c, BAR_RAW_EMPTY + rs));
+                }
             }
             if (dw == 0 && lane < kRawPerTile)
-                st_shared_u32(c.sb + kOffXMask + (xs * kRawPerTile + lane) * 4, lane == 0 ? mask[0] : mask[1]);
+                st_shared_u32(c.sb + kOffXMask + (xs * kRawPerTile + lane) * 4, lane == 0 ? mask0 : mask1);
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) vbound = fmaxf(vbound, __shfl_xor_sync(0xffffffffu, vbound, o));
             if (lane == 0) st_shared_f32(c.sb + kOffXVmax + (xs * kNumDequantWarps + dw) * 4, vbound);
@@ -658,26 +665,27 @@ __device__ void mma_role(const Ctx& c, const UnitDesc* units, int n_units) {
             // The peer dims' K steps go first (the dequant writes them first) and
             // their completion frees the peer buffer, so the dequant of the next
             // tile's peer dims overlaps the own dims' K steps.
-#pragma unroll
+#pragma unroll 1
             for (int part = 0; part < 2; ++part) {
                 if (part == 1) {
                     if (!wait_bar(c, bar_addr(c, BAR_X_FULL + xs), (g / kNXO) & 1u)) { ok = false; break; }
                     tc_fence_after();
                 }
                 const bool lo_dims = (part == 0) == (c.half == 1);  // dims 0..255 are peer dims for half 1
-                if (lo_dims) {
-#pragma unroll
-                    for (int kk = 0; kk < 16; ++kk) {
-                        const uint64_t bd = lo_desc + (uint64_t)(((kk >> 2) * kAtomBytes + (kk & 3) * 32) >> 4);
-                        mma_bf16_ts(ts, c.tmem + kTmemQ + kk * 8, bd, idesc_qk, (part == 0 && kk == 0) ? 0u : 1u);
-                    }
-                } else {
-#pragma unroll
-                    for (int kk = 0; kk < 16; ++kk) {
-                        const uint64_t ad = q_desc0 + (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-                        const uint64_t bd = hi_desc + (uint64_t)(((kk >> 2) * kAtomBytes + (kk & 3) * 32) >> 4);
-                        mma_bf16_ss(ts, ad, bd, idesc_qk, (part == 0 && kk == 0) ? 0u : 1u);
-                    }
+                const uint32_t acc0 = part == 0 ? 0u : 1u;
+                if (lo_dims) {  // dims 0..255: Q from TMEM
+                    const uint64_t bd0 = lo_desc;
+#pragma unroll 4
+                    for (int kk = 0; kk < 16; ++kk)
+                        mma_bf16_ts(ts, c.tmem + kTmemQ + kk * 8,
+                                    bd0 + (uint64_t)(((kk >> 2) * kAtomBytes + (kk & 3) * 32) >> 4), idesc_qk,
+                                    kk == 0 ? acc0 : 1u);
+                } else {  // dims 256..511: Q from shared memory
+#pragma unroll 4
+                    for (int kk = 0; kk < 16; ++kk)
+                        mma_bf16_ss(ts, q_desc0 + (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4),
+                                    hi_desc + (uint64_t)(((kk >> 2) * kAtomBytes + (kk & 3) * 32) >> 4), idesc_qk,
+                                    kk == 0 ? acc0 : 1u);
                 }
                 if (part == 0) {
                     mma_commit(bar_addr(c, BAR_XP_EMPTY));
@@ -770,7 +778,7 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, const UnitDesc* uni
             // pass 1: the tile's masked maximum (scores are reloaded in pass 2, so
             // only 32 of them are live at a time)
             float mt = -INFINITY;
-#pragma unroll
+#pragma unroll 1
             for (int hf = 0; hf < 2; ++hf) {
                 uint32_t v[32];
                 tmem_ld32(ts + 32 * hf, v);
