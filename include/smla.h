@@ -106,9 +106,13 @@ typedef struct smla_decode_args {
     int32_t num_rows;            /* 1 .. SMLA_MAX_ROWS                                               */
     int32_t num_heads;           /* 1 .. SMLA_MAX_HEADS                                              */
     int32_t num_splits;          /* 1 .. SMLA_MAX_SPLITS: split budget per row (from the planner).
-                                    The grid holds num_rows*num_splits work units; the kernel hands
-                                    them to rows in proportion to each row's live length.  Keep it
-                                    fixed across CUDA-graph replays (it sizes the grid).            */
+                                    The kernel's chunked plan uses at most num_rows*num_splits work
+                                    units, handed to rows in proportion to each row's live length;
+                                    its stream plan instead cuts the rows' tiles, laid end to end,
+                                    into one equal range per CTA pair (a row crossing a cut is
+                                    merged from its parts).  The kernel takes whichever plan has the
+                                    smaller estimated time, from the live lengths.  Keep num_splits
+                                    fixed across CUDA-graph replays.                                 */
 } smla_decode_args;
 
 /*
@@ -146,7 +150,9 @@ int smla_plan_num_splits_ex(int num_rows, int num_heads, int64_t kv_len,
  * split budget of max_splits (cf. the persistent kernel's workspace getter in
  * aiter pull request 6126, summary part 2).  The layout is: a device error
  * word, per-(row, half) arrival counters, per-unit fp32 partial (m, l) and
- * per-unit fp32 partial O.  Allocate it once, zero it once (cudaMemset 0),
+ * per-unit fp32 partial O, for max(max_rows * max_splits, max_rows + 95)
+ * units (the second term lets the stream plan use up to 96 CTA pairs).
+ * Allocate it once, zero it once (cudaMemset 0),
  * outside any graph capture; every successful call leaves the counters back
  * at zero, so it can be reused across calls and batch sizes.  Returns 0 for
  * arguments out of range.
@@ -155,7 +161,8 @@ size_t smla_workspace_bytes(int max_rows, int num_heads, int max_splits);
 
 /*
  * One decode step: validates on the host, then enqueues ONE kernel launch on
- * `stream` (a grid of num_rows*num_splits CTA pairs, cluster size 2).
+ * `stream`: a persistent grid of CTA pairs (one CTA per output dim half), as
+ * many as are co-resident on the device.
  * Host checks come first: NULL or misaligned pointers, unsupported sizes, a
  * workspace smaller than smla_workspace_bytes(num_rows, num_heads, num_splits)
  * and a device that is not sm_103 each return an error and launch nothing.

@@ -79,6 +79,9 @@ constexpr int kHeadsPad = 128;        // heads padded up to the MMA M
 static_assert(kHeadsPad == 32 * kSoftmaxWarps, "one softmax thread per padded head");
 static_assert(kRawBK == 32, "one producer lane per slot");
 constexpr int kMaxUnitsPerPair = 32;
+constexpr int kUnitCostTiles = 2;     // plan estimate: staging + finishing a unit, in tiles
+constexpr int kMinStreamTiles = 4;    // a stream-plan range is at least this many tiles
+constexpr int kMaxStreamRanges = 96;  // stream-plan ranges (pairs) at most: bounds a row's partials
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;        // O half: columns [0, 256)
@@ -115,9 +118,12 @@ constexpr uint32_t kOffUnits = kOffMisc + kMiscBytes;           // unit descript
 constexpr uint32_t kSmemUsed = kOffUnits + kMaxUnitsPerPair * 32;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;               // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
+// merge weights [s_r][H] fit in the own + peer stages for any s_r the plans make
+static_assert((kNXO + 1) * kHalfBytes >= 4 * SMLA_MAX_HEADS * (SMLA_MAX_SPLITS > kMaxStreamRanges ? SMLA_MAX_SPLITS : kMaxStreamRanges),
+              "merge weights fit");
 // The plan's per-row scratch (tiles[R], prefix[R+1]) aliases the raw ring
 // during the prologue, before any producer runs.
-static_assert(4 * (2 * SMLA_MAX_ROWS + 8) <= kNR * kRawStageBytes, "plan scratch fits in the raw ring");
+static_assert(4 * (3 * SMLA_MAX_ROWS + 8) <= kNR * kRawStageBytes, "plan scratch fits in the raw ring");
 
 // mbarrier indices
 enum : uint32_t {
@@ -142,11 +148,14 @@ struct KParams {
     uint32_t* counters;  // [SMLA_MAX_ROWS][2]
     float2* ml;          // [units][2][H]   (m in log2 units, l)
     float* po;           // [units][H][512] unnormalised fp32 O
-    int units;           // num_rows * num_splits (work units of the plan)
+    int units;           // num_rows * num_splits: the chunked plan's unit budget
+    int unit_cap;        // partial slots in the workspace (>= units and >= rows + kMaxPairs - 1)
 };
 
 struct UnitDesc {
-    int row, s_r, row_u0, unit, t_begin, t_end, pad0, pad1;
+    int row, s_r, row_u0, unit, t_begin, t_end;
+    int pad0;  // set to 1 when this CTA arrived last at the unit's row and owes its merge
+    int pad1;
 };
 
 // ---------------------------------------------------------------------------
@@ -711,7 +720,7 @@ __device__ void mma_role(const Ctx& c, const UnitDesc* units, int n_units) {
 // ---------------------------------------------------------------------------
 // role: softmax / epilogue (warps 0-3, thread = head = TMEM lane)
 // ---------------------------------------------------------------------------
-__device__ void softmax_role(const KParams& p, const Ctx& c, const UnitDesc* units, int n_units, uint32_t& err) {
+__device__ void softmax_role(const KParams& p, const Ctx& c, UnitDesc* units, int n_units, uint32_t& err) {
     const smla_decode_args& a = p.a;
     const int h = threadIdx.x;  // 0..127
     const int warp = threadIdx.x >> 5;
@@ -729,29 +738,51 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, const UnitDesc* uni
         const UnitDesc d = units[ui];
         const int r = d.row;
         const int n = d.t_end - d.t_begin;
-        // ---- Q of this row: dims 0..255 -> TMEM [320, 448) as bf16 pairs,
-        //      dims 256..511 -> shared memory, K-major with the 128-byte swizzle ----
+        // ---- Q of this row: dims 0..255 -> TMEM [384, 512) as bf16 pairs,
+        //      dims 256..511 -> shared memory, K-major with the 128-byte swizzle.
+        //      The next unit's q rows are prefetched into L2 now, a unit ahead.
         {
-            const size_t hq = (size_t)r * H + (h < H ? h : 0);
-            const uint16_t* qn = static_cast<const uint16_t*>(a.q_nope) + hq * SMLA_NOPE_DIMS;
-            const uint16_t* qr = static_cast<const uint16_t*>(a.q_rope) + hq * SMLA_ROPE_DIMS;
-#pragma unroll 1
-            for (int cc = 0; cc < 4; ++cc) {  // dims 64cc .. 64cc+63 -> 32 TMEM columns
-                uint32_t v[32];
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    uint4 w = make_uint4(0u, 0u, 0u, 0u);
-                    if (h < H) w = __ldg(reinterpret_cast<const uint4*>(qn + (cc * 8 + q) * 8));
-                    v[4 * q] = w.x; v[4 * q + 1] = w.y; v[4 * q + 2] = w.z; v[4 * q + 3] = w.w;
-                }
-                tmem_st32(c.tmem + kTmemQ + lane_base + 32 * cc, v);
+            if (h == 0 && ui + 1 < n_units) {
+                const size_t rn = (size_t)units[ui + 1].row * H;
+                bulk_prefetch_l2(static_cast<const uint16_t*>(a.q_nope) + rn * SMLA_NOPE_DIMS,
+                                 (uint32_t)(H * SMLA_NOPE_DIMS * 2));
+                bulk_prefetch_l2(static_cast<const uint16_t*>(a.q_rope) + rn * SMLA_ROPE_DIMS,
+                                 (uint32_t)(H * SMLA_ROPE_DIMS * 2));
             }
-#pragma unroll 4
-            for (int k = 0; k < 32; ++k) {  // dims 256 + 8k .. : NoPE 256..447, then RoPE 0..63
-                uint4 w = make_uint4(0u, 0u, 0u, 0u);
-                if (h < H) w = k < 24 ? __ldg(reinterpret_cast<const uint4*>(qn + 256 + k * 8))
-                                      : __ldg(reinterpret_cast<const uint4*>(qr + (k - 24) * 8));
-                st_shared_v4(c.sb + kOffQ + (k >> 3) * 16384 + sw128_offset(h, k & 7), w.x, w.y, w.z, w.w);
+            const size_t hq = (size_t)r * H + (h < H ? h : 0);
+            const uint4* qn = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q_nope) + hq * SMLA_NOPE_DIMS);
+            const uint4* qr = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q_rope) + hq * SMLA_ROPE_DIMS);
+            // 16 loads in flight per batch: dims 0..255 in two batches
+#pragma unroll 1
+            for (int bt = 0; bt < 2; ++bt) {
+                uint4 w[16];
+#pragma unroll
+                for (int q = 0; q < 16; ++q) w[q] = h < H ? __ldg(qn + 16 * bt + q) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                for (int hc = 0; hc < 2; ++hc) {  // dims 128 bt + 64 hc .. : 32 TMEM columns
+                    uint32_t v[32];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        v[4 * q] = w[8 * hc + q].x; v[4 * q + 1] = w[8 * hc + q].y;
+                        v[4 * q + 2] = w[8 * hc + q].z; v[4 * q + 3] = w[8 * hc + q].w;
+                    }
+                    tmem_st32(c.tmem + kTmemQ + lane_base + 32 * (2 * bt + hc), v);
+                }
+            }
+            // dims 256..511 (NoPE 256..447, then RoPE 0..63): 16-byte chunk k = 8 dims
+#pragma unroll 1
+            for (int bt = 0; bt < 2; ++bt) {
+                uint4 w[16];
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                    const int k = 16 * bt + q;
+                    w[q] = h >= H ? make_uint4(0u, 0u, 0u, 0u) : (k < 24 ? __ldg(qn + 32 + k) : __ldg(qr + (k - 24)));
+                }
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                    const int k = 16 * bt + q;
+                    st_shared_v4(c.sb + kOffQ + (k >> 3) * 16384 + sw128_offset(h, k & 7), w[q].x, w[q].y, w[q].z, w[q].w);
+                }
             }
             fence_proxy_async_smem();
             tmem_wait_st();
@@ -941,61 +972,9 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, const UnitDesc* uni
                 *flag = (old == (uint32_t)(d.s_r - 1)) ? 1u : 0u;
             }
             softmax_bar();
-            if (*flag != 0u) {
-                __threadfence();
-                if (h < H) {
-                    float M = sink2;
-                    for (int i = 0; i < d.s_r; ++i)
-                        M = fmaxf(M, __ldcg(p.ml + ((size_t)(d.row_u0 + i) * 2 + c.half) * H + h).x);
-                    float Z = 0.f, lall = 0.f;
-                    if (M != -INFINITY) {
-                        Z = (sink2 == -INFINITY) ? 0.f : exp2f(sink2 - M);
-                        for (int i = 0; i < d.s_r; ++i) {
-                            const float2 ml = __ldcg(p.ml + ((size_t)(d.row_u0 + i) * 2 + c.half) * H + h);
-                            if (ml.x != -INFINITY) Z += ml.y * exp2f(ml.x - M);
-                            lall += ml.y;
-                        }
-                    }
-                    const float inv = Z > 0.f ? 1.f / Z : 0.f;
-                    uint16_t* outp = static_cast<uint16_t*>(a.out) + ((size_t)r * H + h) * SMLA_HEAD_DIM + 256 * c.half;
-#pragma unroll 1
-                    for (int cc = 0; cc < 8; ++cc) {
-                        float acc[32];
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) acc[j] = 0.f;
-                        for (int i = 0; i < d.s_r; ++i) {
-                            const size_t u = (size_t)(d.row_u0 + i);
-                            const float mi = __ldcg(p.ml + (u * 2 + c.half) * H + h).x;
-                            if (mi == -INFINITY) continue;
-                            const float w = exp2f(mi - M) * inv;
-                            const float* src = p.po + (u * H + h) * SMLA_HEAD_DIM + 256 * c.half + 32 * cc;
-#pragma unroll
-                            for (int q = 0; q < 8; ++q) {
-                                const float4 v = __ldcg(reinterpret_cast<const float4*>(src + 4 * q));
-                                acc[4 * q] += w * v.x;
-                                acc[4 * q + 1] += w * v.y;
-                                acc[4 * q + 2] += w * v.z;
-                                acc[4 * q + 3] += w * v.w;
-                            }
-                        }
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            uint4 wv;
-                            wv.x = pack_bf16(acc[8 * q], acc[8 * q + 1]);
-                            wv.y = pack_bf16(acc[8 * q + 2], acc[8 * q + 3]);
-                            wv.z = pack_bf16(acc[8 * q + 4], acc[8 * q + 5]);
-                            wv.w = pack_bf16(acc[8 * q + 6], acc[8 * q + 7]);
-                            *reinterpret_cast<uint4*>(outp + 32 * cc + 8 * q) = wv;
-                        }
-                    }
-                    if (c.half == 0 && a.lse != nullptr) {
-                        float lse = (M == -INFINITY || Z <= 0.f) ? -INFINITY : (M + log2f(Z)) * kLn2;
-                        if (lall == 0.f) lse = a.sink != nullptr ? __ldg(a.sink + h) : -INFINITY;  // sink only, exactly
-                        a.lse[(size_t)r * H + h] = lse;
-                    }
-                }
-                if (h == 0) atomicExch(p.counters + 2 * r + c.half, 0u);
-            }
+            // The last arriver merges the row's partials, but only after its
+            // own units are done, with every warp of the CTA (merge_rows).
+            if (h == 0 && *flag != 0u) units[ui].pad0 = 1;
         }
         // All TMEM reads of O are complete (tcgen05.wait::ld) before the next
         // unit's Q is staged; its first PV (which overwrites O) waits for Q.
@@ -1003,6 +982,133 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, const UnitDesc* uni
         softmax_bar();
     }
     if (!ok) err |= SMLA_DEV_TIMEOUT;
+}
+
+// ---------------------------------------------------------------------------
+// merge of a split row's partials (this CTA's dims half), run by all threads
+// after the CTA's units are done, so that the pipeline's shared memory is free
+// ---------------------------------------------------------------------------
+// Per head: M = max(sink, m_i), Z = sum_i l_i 2^(m_i - M) + 2^(sink - M),
+// out = sum_i 2^(m_i - M) O_i / Z, lse = (M + log2 Z) ln 2, in split order.
+// Partials with m = -inf saw no entry; their O is never read.
+__device__ void merge_row(const KParams& p, const Ctx& c, const UnitDesc& d, float* s_w, float* s_inv) {
+    const smla_decode_args& a = p.a;
+    const int H = a.num_heads, tid = threadIdx.x;
+    const int sr = d.s_r, r = d.row;
+    // pass 1: one thread per head computes the weights 2^(m_i - M) and 1 / Z
+    for (int h = tid; h < H; h += kThreads) {
+        const float sink2 = a.sink != nullptr ? __ldg(a.sink + h) * kLog2e : -INFINITY;
+        float M = sink2;
+        for (int i = 0; i < sr; ++i) M = fmaxf(M, __ldcg(p.ml + ((size_t)(d.row_u0 + i) * 2 + c.half) * H + h).x);
+        float Z = 0.f, lall = 0.f;
+        if (M != -INFINITY) Z = (sink2 == -INFINITY) ? 0.f : exp2f(sink2 - M);
+        for (int i = 0; i < sr; ++i) {
+            const float2 ml = __ldcg(p.ml + ((size_t)(d.row_u0 + i) * 2 + c.half) * H + h);
+            const bool use = ml.x != -INFINITY;
+            if (M != -INFINITY && use) Z += ml.y * exp2f(ml.x - M);
+            lall += ml.y;
+            s_w[i * H + h] = use ? exp2f(ml.x - M) : 0.f;  // exact 0 marks "not read"
+            if (!use) s_w[i * H + h] = -1.f;
+        }
+        s_inv[h] = Z > 0.f ? 1.f / Z : 0.f;
+        if (c.half == 0 && a.lse != nullptr) {
+            float lse = (M == -INFINITY || Z <= 0.f) ? -INFINITY : (M + log2f(Z)) * kLn2;
+            if (lall == 0.f) lse = a.sink != nullptr ? __ldg(a.sink + h) : -INFINITY;  // sink only, exactly
+            a.lse[(size_t)r * H + h] = lse;
+        }
+    }
+    __syncthreads();
+    // pass 2: item = (head, 16 dims); all of an item's loads are in flight together
+    const int items = H * 16;
+    for (int it = tid; it < items; it += kThreads) {
+        const int h = it >> 4, q16 = it & 15;
+        const float inv = s_inv[h];
+        float acc[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) acc[j] = 0.f;
+#pragma unroll 1
+        for (int i = 0; i < sr; i += 4) {
+            float4 v[4][4];
+            float w[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int ii = min(i + k, sr - 1);
+                const float* src = p.po + ((size_t)(d.row_u0 + ii) * H + h) * SMLA_HEAD_DIM + 256 * c.half + 16 * q16;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) v[k][q] = __ldcg(reinterpret_cast<const float4*>(src + 4 * q));
+                w[k] = (i + k < sr) ? s_w[ii * H + h] : -1.f;
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const bool use = w[k] >= 0.f;
+                const float wk = use ? w[k] * inv : 0.f;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    acc[4 * q] = use ? acc[4 * q] + wk * v[k][q].x : acc[4 * q];
+                    acc[4 * q + 1] = use ? acc[4 * q + 1] + wk * v[k][q].y : acc[4 * q + 1];
+                    acc[4 * q + 2] = use ? acc[4 * q + 2] + wk * v[k][q].z : acc[4 * q + 2];
+                    acc[4 * q + 3] = use ? acc[4 * q + 3] + wk * v[k][q].w : acc[4 * q + 3];
+                }
+            }
+        }
+        uint16_t* outp = static_cast<uint16_t*>(a.out) + ((size_t)r * H + h) * SMLA_HEAD_DIM + 256 * c.half + 16 * q16;
+        uint4 w0, w1;
+        w0.x = pack_bf16(acc[0], acc[1]); w0.y = pack_bf16(acc[2], acc[3]);
+        w0.z = pack_bf16(acc[4], acc[5]); w0.w = pack_bf16(acc[6], acc[7]);
+        w1.x = pack_bf16(acc[8], acc[9]); w1.y = pack_bf16(acc[10], acc[11]);
+        w1.z = pack_bf16(acc[12], acc[13]); w1.w = pack_bf16(acc[14], acc[15]);
+        reinterpret_cast<uint4*>(outp)[0] = w0;
+        reinterpret_cast<uint4*>(outp)[1] = w1;
+    }
+    __syncthreads();
+    if (tid == 0) atomicExch(p.counters + 2 * r + c.half, 0u);
+}
+
+// ---------------------------------------------------------------------------
+// plan helpers (prologue, all threads of the CTA)
+// ---------------------------------------------------------------------------
+// out[r] = sum of f(r') for r' < r, r < R, and out[R] = the total.  Thread t
+// takes a contiguous block of rows; `red` is CTA scratch of kWarps entries.
+template <class F>
+__device__ void block_exclusive_scan(int R, const int* /*unused*/, int* out, long long* red, F f) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int per = (R + kThreads - 1) / kThreads;
+    int my_sum = 0;
+    for (int r = tid * per; r < min(R, (tid + 1) * per); ++r) my_sum += f(r);
+    int incl = my_sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    __syncthreads();
+    if (lane == 31) red[warp] = incl;
+    __syncthreads();
+    int base = 0;
+    for (int w = 0; w < warp; ++w) base += (int)red[w];
+    int run = base + incl - my_sum;
+    for (int r = tid * per; r < min(R, (tid + 1) * per); ++r) {
+        out[r] = run;
+        run += f(r);
+    }
+    if (tid == kThreads - 1) out[R] = run;
+    __syncthreads();
+}
+
+// The row holding tile position pos of the concatenated stream (the last r
+// with cum[r] <= pos; rows with no tile are skipped over by cum).
+__device__ __forceinline__ int row_of_tile(const int* cum, int R, long long pos) {
+    int lo = 0, hi = R - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (cum[mid] <= pos) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+// The stream range q (of Q equal ranges [q T / Q, (q + 1) T / Q)) holding pos.
+__device__ __forceinline__ int stream_range_of(long long pos, long long T, int Q) {
+    return (int)(((pos + 1) * Q - 1) / T);
 }
 
 // ---------------------------------------------------------------------------
@@ -1020,7 +1126,8 @@ __global__ void __launch_bounds__(kThreads, 1) smla_decode_kernel(const KParams 
     c.abort = misc + 1;
     long long* red = reinterpret_cast<long long*>(smem + kOffMisc + 64);
     int* s_tiles = reinterpret_cast<int*>(smem + kOffRaw);  // prologue only
-    int* s_prefix = s_tiles + SMLA_MAX_ROWS;
+    int* s_prefix = s_tiles + SMLA_MAX_ROWS;                 // [R + 1]
+    int* s_cum = s_prefix + SMLA_MAX_ROWS + 1;               // [R + 1]
     UnitDesc* units = reinterpret_cast<UnitDesc*>(smem + kOffUnits);
     const int R = a.num_rows;
     const int pair = blockIdx.x >> 1;
@@ -1054,11 +1161,18 @@ __global__ void __launch_bounds__(kThreads, 1) smla_decode_kernel(const KParams 
     }
 
     // ---- in-kernel split plan (identical in every CTA; reads live lengths) ----
-    // tiles_r per row; smallest chunk c with sum_r max(1, ceil(tiles_r / c)) <= budget;
-    // row r gets s_r = ceil(tiles_r / ceil(tiles_r / ceil(tiles_r / c))) splits.
-    // The budget is the caller's rows * num_splits, rounded down to a whole
-    // number of passes over the grid's CTA pairs when it exceeds one pass, so
-    // that no pair is handed one more unit than the others.
+    // Two candidates, chosen by an estimated makespan in tiles (each unit also
+    // costs about kUnitCostTiles of staging and finishing):
+    //  (a) chunked: tiles_r per row; smallest chunk c with
+    //      sum_r max(1, ceil(tiles_r / c)) <= budget; row r gets
+    //      s_r = ceil(tiles_r / ceil(tiles_r / ceil(tiles_r / c))) equal splits and
+    //      pair p takes units p, p + n_pairs, ...  The budget is the caller's
+    //      rows * num_splits, rounded down to a whole number of passes over the
+    //      grid's pairs when it exceeds one pass.
+    //  (b) stream: the rows' tiles laid end to end and cut into Q equal ranges,
+    //      one per pair; a row crossing a cut gets one unit per range it meets
+    //      (at most rows + Q - 1 units, which the workspace always holds).  Rows
+    //      with no tile get one empty unit each, on pair r % Q.
     const int budget = max(R, p.units > n_pairs ? (p.units / n_pairs) * n_pairs : p.units);
     uint32_t plan_err = 0;
     int local_max = 0;
@@ -1089,58 +1203,114 @@ __global__ void __launch_bounds__(kThreads, 1) smla_decode_kernel(const KParams 
         if (tot <= budget) hi = mid; else lo = mid + 1;
     }
     const int chunk = lo;
-    const int per = (R + kThreads - 1) / kThreads;
-    int my_sum = 0;
-    for (int r = tid * per; r < min(R, (tid + 1) * per); ++r) {
+    // exclusive scans over rows: s_cum (tiles) and s_prefix (chunked units)
+    block_exclusive_scan(R, s_tiles, s_cum, red, [&](int r) { return s_tiles[r]; });
+    block_exclusive_scan(R, s_tiles, s_prefix, red, [&](int r) {
         const int t = s_tiles[r];
-        int s = max(1, ceil_div_i(t, chunk));
-        if (t > 0) s = ceil_div_i(t, ceil_div_i(t, s));
-        my_sum += s;
-    }
-    int incl = my_sum;
+        int sr = max(1, ceil_div_i(t, chunk));
+        if (t > 0) sr = ceil_div_i(t, ceil_div_i(t, sr));
+        return sr;
+    });
+    const long long T = s_cum[R];
+    const int units_c = s_prefix[R];
+    // candidate (b): Q ranges, each at least kMinStreamTiles tiles long
+    int Q = min(min(n_pairs, p.unit_cap - R + 1), kMaxStreamRanges);
+    Q = (int)min((long long)Q, max(1LL, T / kMinStreamTiles));
+    bool stream = false;
+    if (Q > 1 && T > 0 && Q > min(units_c, n_pairs)) {
+        // upper bound on any pair's unit count: rows met by its range + empty rows
+        int zero_rows = 0, upp = 0;
+        for (int r = tid; r < R; r += kThreads) zero_rows += s_tiles[r] == 0;
+        for (int q = tid; q < Q; q += kThreads) {
+            const long long ra = q * T / Q, rb = (q + 1) * T / Q;
+            if (ra < rb) upp = max(upp, row_of_tile(s_cum, R, rb - 1) - row_of_tile(s_cum, R, ra) + 1);
+        }
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
+        for (int o = 16; o > 0; o >>= 1) {
+            zero_rows += __shfl_xor_sync(0xffffffffu, zero_rows, o);
+            upp = max(upp, __shfl_xor_sync(0xffffffffu, upp, o));
+        }
+        __syncthreads();
+        if (lane == 0) { red[warp] = zero_rows; red[16 + warp] = upp; }
+        __syncthreads();
+        long long zr = 0;
+        int up = 0;
+        for (int w = 0; w < kWarps; ++w) { zr += red[w]; up = max(up, (int)red[16 + w]); }
+        up += (int)min(zr, (long long)((R + Q - 1) / Q));  // empty rows r = q, q + Q, ... of one pair
+        const long long passes_c = (units_c + n_pairs - 1) / n_pairs;
+        const long long mk_c = (long long)chunk * passes_c + kUnitCostTiles * passes_c;
+        const long long mk_s = (T + Q - 1) / Q + (long long)kUnitCostTiles * up;
+        stream = up <= kMaxUnitsPerPair && mk_s < mk_c;
     }
-    __syncthreads();
-    if (lane == 31) red[warp] = incl;
-    __syncthreads();
-    int base = 0;
-    for (int w = 0; w < warp; ++w) base += (int)red[w];
-    int run = base + incl - my_sum;
-    for (int r = tid * per; r < min(R, (tid + 1) * per); ++r) {
-        s_prefix[r] = run;
-        const int t = s_tiles[r];
-        int s = max(1, ceil_div_i(t, chunk));
-        if (t > 0) s = ceil_div_i(t, ceil_div_i(t, s));
-        run += s;
+    if (stream) {
+        // per-row unit counts of the stream plan, then their prefix (unit ids)
+        block_exclusive_scan(R, s_tiles, s_prefix, red, [&](int r) {
+            const int t = s_tiles[r];
+            if (t == 0) return 1;
+            return stream_range_of(s_cum[r + 1] - 1, T, Q) - stream_range_of(s_cum[r], T, Q) + 1;
+        });
     }
-    if (tid == kThreads - 1) s_prefix[R] = run;
-    __syncthreads();
     const int total_units = s_prefix[R];
-    // this pair's units: pair, pair + n_pairs, ...
     if (tid == 0) {
         int n = 0;
-        for (int u = pair; u < total_units && n < kMaxUnitsPerPair; u += n_pairs, ++n) {
-            int l2 = 0, h2 = R - 1;  // last r with prefix[r] <= u
-            while (l2 < h2) {
-                const int mid = (l2 + h2 + 1) >> 1;
-                if (s_prefix[mid] <= u) l2 = mid; else h2 = mid - 1;
+        if (stream) {
+            if (pair < Q) {
+                const long long ra = pair * T / Q, rb = (pair + 1) * T / Q;
+                if (ra < rb) {
+                    for (int r = row_of_tile(s_cum, R, ra); r < R && s_cum[r] < rb; ++r) {
+                        if (s_tiles[r] == 0) continue;
+                        const int q0 = stream_range_of(s_cum[r], T, Q);
+                        UnitDesc d;
+                        d.row = r;
+                        d.row_u0 = s_prefix[r];
+                        d.s_r = s_prefix[r + 1] - d.row_u0;
+                        d.unit = d.row_u0 + (pair - q0);
+                        d.t_begin = (int)(max(ra, (long long)s_cum[r]) - s_cum[r]);
+                        d.t_end = (int)(min(rb, (long long)s_cum[r + 1]) - s_cum[r]);
+                        d.pad0 = d.pad1 = 0;
+                        if (n < kMaxUnitsPerPair) units[n++] = d;
+                    }
+                }
+                for (int r = pair; r < R; r += Q) {
+                    if (s_tiles[r] != 0) continue;
+                    UnitDesc d;
+                    d.row = r;
+                    d.row_u0 = d.unit = s_prefix[r];
+                    d.s_r = 1;
+                    d.t_begin = d.t_end = 0;
+                    d.pad0 = d.pad1 = 0;
+                    if (n < kMaxUnitsPerPair) units[n++] = d;
+                }
             }
-            UnitDesc d;
-            d.row = l2;
-            d.row_u0 = s_prefix[l2];
-            d.s_r = s_prefix[l2 + 1] - d.row_u0;
-            d.unit = u;
-            const int T = s_tiles[l2];
-            const int tps = T > 0 ? ceil_div_i(T, d.s_r) : 0;
-            d.t_begin = min(T, (u - d.row_u0) * tps);
-            d.t_end = min(T, d.t_begin + tps);
-            d.pad0 = d.pad1 = 0;
-            units[n] = d;
+        } else {
+            // this pair's units: pair, pair + n_pairs, ...
+            for (int u = pair; u < total_units && n < kMaxUnitsPerPair; u += n_pairs, ++n) {
+                int l2 = 0, h2 = R - 1;  // last r with prefix[r] <= u
+                while (l2 < h2) {
+                    const int mid = (l2 + h2 + 1) >> 1;
+                    if (s_prefix[mid] <= u) l2 = mid; else h2 = mid - 1;
+                }
+                UnitDesc d;
+                d.row = l2;
+                d.row_u0 = s_prefix[l2];
+                d.s_r = s_prefix[l2 + 1] - d.row_u0;
+                d.unit = u;
+                const int Tr = s_tiles[l2];
+                const int tps = Tr > 0 ? ceil_div_i(Tr, d.s_r) : 0;
+                d.t_begin = min(Tr, (u - d.row_u0) * tps);
+                d.t_end = min(Tr, d.t_begin + tps);
+                d.pad0 = d.pad1 = 0;
+                units[n] = d;
+            }
         }
         misc[2] = (uint32_t)n;
+        if (n > 0) {  // the first unit's q rows start their trip to L2 now
+            const size_t r0 = (size_t)units[0].row * a.num_heads;
+            bulk_prefetch_l2(static_cast<const uint16_t*>(a.q_nope) + r0 * SMLA_NOPE_DIMS,
+                             (uint32_t)(a.num_heads * SMLA_NOPE_DIMS * 2));
+            bulk_prefetch_l2(static_cast<const uint16_t*>(a.q_rope) + r0 * SMLA_ROPE_DIMS,
+                             (uint32_t)(a.num_heads * SMLA_ROPE_DIMS * 2));
+        }
     }
     if (blockIdx.x == 0 && plan_err) err |= plan_err;
     tc_fence_before();
@@ -1162,9 +1332,20 @@ __global__ void __launch_bounds__(kThreads, 1) smla_decode_kernel(const KParams 
     }
 
     if (*c.abort) err |= SMLA_DEV_TIMEOUT;
-    if (err != 0u) atomicOr(p.err, err);
     tc_fence_before();
     __syncthreads();
+    // Merges this CTA owes (it arrived last at those rows), with every warp;
+    // the pipeline's shared memory is free now and holds the weights.
+    if (*c.abort == 0u) {
+        float* s_w = reinterpret_cast<float*>(smem + kOffXO);    // [s_r][H] partial weights (own + peer stages)
+        float* s_inv = reinterpret_cast<float*>(smem + kOffRaw);  // [H] 1 / Z (raw ring)
+        for (int ui = 0; ui < n_units; ++ui) {
+            if (units[ui].pad0 == 0) continue;
+            __threadfence();
+            merge_row(p, c, units[ui], s_w, s_inv);
+        }
+    }
+    if (err != 0u) atomicOr(p.err, err);
     if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(c.tmem, kTmemCols);
@@ -1210,11 +1391,12 @@ smla_status launch_decode(const smla_decode_args* args, void* workspace, cudaStr
     kp.ml = reinterpret_cast<float2*>(ws + L.off_ml);
     kp.po = reinterpret_cast<float*>(ws + L.off_po);
     kp.units = args->num_rows * args->num_splits;
+    kp.unit_cap = unit_capacity(args->num_rows, args->num_splits);
     // Persistent grid: CTA pairs (one CTA per output half) up to what is
-    // co-resident, at most one pair per unit, and enough pairs that none is
-    // handed more than kMaxUnitsPerPair units.
+    // co-resident (the stream plan can use every one of them), and enough
+    // pairs that the chunked plan hands none more than kMaxUnitsPerPair units.
     const int pairs_resident = std::max(1, g_resident[dev].load(std::memory_order_relaxed) / 2);
-    int pairs = std::min(kp.units, pairs_resident);
+    int pairs = std::min(kp.unit_cap, pairs_resident);
     pairs = std::max(pairs, (kp.units + kMaxUnitsPerPair - 1) / kMaxUnitsPerPair);
     const dim3 grid((unsigned)(2 * pairs)), block(kThreads);
     smla_decode_kernel<<<grid, block, kSmemBytes, stream>>>(kp);

@@ -14,15 +14,24 @@ struct WorkspaceLayout {
     size_t off_err;       // uint32 device error word
     size_t off_counters;  // uint32 [SMLA_MAX_ROWS][2] arrival counters (row, dim half)
     size_t off_ml;        // float2 [units][2][H]  per-unit (m, l), one copy per dim half
-    size_t off_po;        // float  [units][H][512] per-unit unnormalised O
+    size_t off_po;        // float  [units][H][512] per-unit unnormalised O (units = unit_capacity)
     size_t total;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Partial slots: rows * splits for the chunked plan, and at least
+// rows + kWorkspacePairs - 1 so that the stream plan (one tile range per CTA
+// pair, up to kWorkspacePairs pairs) always fits.
+constexpr int kWorkspacePairs = 96;
+inline int unit_capacity(int rows, int splits) {
+    const int a = rows * splits, b = rows + kWorkspacePairs - 1;
+    return a > b ? a : b;
+}
+
 inline WorkspaceLayout workspace_layout(int rows, int heads, int splits) {
     WorkspaceLayout L;
-    const size_t units = (size_t)rows * (size_t)splits;
+    const size_t units = (size_t)unit_capacity(rows, splits);
     L.off_err = 0;
     L.off_counters = 256;
     L.off_ml = align_up(L.off_counters + sizeof(uint32_t) * 2 * SMLA_MAX_ROWS, 256);

@@ -37,10 +37,14 @@ def test_status_strings(smla_lib):
 
 
 def test_workspace_bytes(smla_lib):
-    a = S.smla_workspace_bytes(32, 128, 2)
-    b = S.smla_workspace_bytes(32, 128, 4)
+    a = S.smla_workspace_bytes(32, 128, 8)
+    b = S.smla_workspace_bytes(32, 128, 10)
     assert 0 < a < b
     assert b - a == 32 * 2 * 128 * (512 * 4 + 2 * 8)
+    # at least rows + 95 partial slots, whatever the split budget
+    unit = 128 * (512 * 4 + 2 * 8)
+    assert S.smla_workspace_bytes(32, 128, 1) == S.smla_workspace_bytes(32, 128, 3)
+    assert S.smla_workspace_bytes(32, 128, 4) - S.smla_workspace_bytes(32, 128, 1) == (128 - 127) * unit
     assert S.smla_workspace_bytes(0, 128, 1) == 0
     assert S.smla_workspace_bytes(1, 129, 1) == 0
     assert S.smla_workspace_bytes(1, 128, 33) == 0
