@@ -119,8 +119,6 @@ constexpr uint32_t kSmemUsed = kOffUnits + kMaxUnitsPerPair * 32;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;               // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 // merge weights [s_r][H] fit in the own + peer stages for any s_r the plans make
-static_assert((kNXO + 1) * kHalfBytes >= 4 * SMLA_MAX_HEADS * (SMLA_MAX_SPLITS > kMaxStreamRanges ? SMLA_MAX_SPLITS : kMaxStreamRanges),
-              "merge weights fit");
 // The plan's per-row scratch (tiles[R], prefix[R+1]) aliases the raw ring
 // during the prologue, before any producer runs.
 static_assert(4 * (3 * SMLA_MAX_ROWS + 8) <= kNR * kRawStageBytes, "plan scratch fits in the raw ring");
@@ -138,7 +136,8 @@ enum : uint32_t {
     BAR_O_DONE = BAR_P_FULL + 2,           // MMA commit after each PV
     BAR_Q_READY = BAR_O_DONE + 1,          // softmax -> MMA, once per unit (kSoftmaxWarps)
     BAR_MMA_FINAL = BAR_Q_READY + 1,       // teardown: all MMAs retired
-    BAR_COUNT = BAR_MMA_FINAL + 1
+    BAR_MERGE = BAR_MMA_FINAL + 1,         // final merges: partials loaded (1 arrival + tx bytes)
+    BAR_COUNT = BAR_MERGE + 1
 };
 static_assert(BAR_COUNT <= kNumBars, "barrier slots");
 
@@ -147,7 +146,7 @@ struct KParams {
     uint32_t* err;
     uint32_t* counters;  // [SMLA_MAX_ROWS][2]
     float2* ml;          // [units][2][H]   (m in log2 units, l)
-    float* po;           // [units][H][512] unnormalised fp32 O
+    float* po;           // [units][2][H][256] unnormalised fp32 O, by dims half
     int units;           // num_rows * num_splits: the chunked plan's unit budget
     int unit_cap;        // partial slots in the workspace (>= units and >= rows + kMaxPairs - 1)
 };
@@ -950,7 +949,7 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, UnitDesc* units, in
             if (c.half == 0 && a.lse != nullptr && h < H) a.lse[(size_t)r * H + h] = lse;
         } else {
             const size_t ub = (size_t)d.unit;
-            float* po = p.po + (ub * H + (h < H ? h : 0)) * SMLA_HEAD_DIM + 256 * c.half;
+            float* po = p.po + ((ub * 2 + c.half) * H + (h < H ? h : 0)) * 256;
 #pragma unroll 1
             for (int cc = 0; cc < 8; ++cc) {
                 uint32_t v[32];
@@ -986,29 +985,44 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, UnitDesc* units, in
 
 // ---------------------------------------------------------------------------
 // merge of a split row's partials (this CTA's dims half), run by all threads
-// after the CTA's units are done, so that the pipeline's shared memory is free
+// after the CTA's units are done, when the pipeline's shared memory is free
 // ---------------------------------------------------------------------------
 // Per head: M = max(sink, m_i), Z = sum_i l_i 2^(m_i - M) + 2^(sink - M),
 // out = sum_i 2^(m_i - M) O_i / Z, lse = (M + log2 Z) ln 2, in split order.
-// Partials with m = -inf saw no entry; their O is never read.
-__device__ void merge_row(const KParams& p, const Ctx& c, const UnitDesc& d, float* s_w, float* s_inv) {
+// Partials with m = -inf saw no entry; their O is never used.  The partials'
+// O rows ([half][H][256] per unit, contiguous) come in by bulk copies, a group
+// of heads of every partial at a time.
+constexpr uint32_t kMergeDataBytes = kOffRaw;                 // [0, kOffRaw): partial O rows
+constexpr uint32_t kOffMergeW = kOffRaw;                      // [s_r][H] float weights
+static_assert(kNR * kRawStageBytes >= 4 * SMLA_MAX_HEADS * (96 + 1) + 8 * SMLA_MAX_HEADS, "merge weights fit");
+
+__device__ void merge_row(const KParams& p, const Ctx& c, const UnitDesc& d, uint32_t& merge_phase) {
     const smla_decode_args& a = p.a;
     const int H = a.num_heads, tid = threadIdx.x;
     const int sr = d.s_r, r = d.row;
-    // pass 1: one thread per head computes the weights 2^(m_i - M) and 1 / Z
+    uint8_t* smem = static_cast<uint8_t*>(__cvta_shared_to_generic(c.sb));
+    float* s_w = reinterpret_cast<float*>(smem + kOffMergeW);  // [sr][H]: weight, or -1 for an unused partial
+    float* s_inv = s_w + sr * H;                                // [H]
+    // pass 1a: every (partial, head) m and l into shared memory at once
+    float2* s_ml = reinterpret_cast<float2*>(smem);  // temporary, in the data area
+    for (int k = tid; k < sr * H; k += kThreads) {
+        const int i = k / H, h = k - i * H;
+        s_ml[k] = __ldcg(p.ml + ((size_t)(d.row_u0 + i) * 2 + c.half) * H + h);
+    }
+    __syncthreads();
+    // pass 1b: one thread per head
     for (int h = tid; h < H; h += kThreads) {
         const float sink2 = a.sink != nullptr ? __ldg(a.sink + h) * kLog2e : -INFINITY;
         float M = sink2;
-        for (int i = 0; i < sr; ++i) M = fmaxf(M, __ldcg(p.ml + ((size_t)(d.row_u0 + i) * 2 + c.half) * H + h).x);
+        for (int i = 0; i < sr; ++i) M = fmaxf(M, s_ml[i * H + h].x);
         float Z = 0.f, lall = 0.f;
         if (M != -INFINITY) Z = (sink2 == -INFINITY) ? 0.f : exp2f(sink2 - M);
         for (int i = 0; i < sr; ++i) {
-            const float2 ml = __ldcg(p.ml + ((size_t)(d.row_u0 + i) * 2 + c.half) * H + h);
+            const float2 ml = s_ml[i * H + h];
             const bool use = ml.x != -INFINITY;
             if (M != -INFINITY && use) Z += ml.y * exp2f(ml.x - M);
             lall += ml.y;
-            s_w[i * H + h] = use ? exp2f(ml.x - M) : 0.f;  // exact 0 marks "not read"
-            if (!use) s_w[i * H + h] = -1.f;
+            s_w[i * H + h] = use ? exp2f(ml.x - M) : -1.f;
         }
         s_inv[h] = Z > 0.f ? 1.f / Z : 0.f;
         if (c.half == 0 && a.lse != nullptr) {
@@ -1018,49 +1032,48 @@ __device__ void merge_row(const KParams& p, const Ctx& c, const UnitDesc& d, flo
         }
     }
     __syncthreads();
-    // pass 2: item = (head, 16 dims); all of an item's loads are in flight together
-    const int items = H * 16;
-    for (int it = tid; it < items; it += kThreads) {
-        const int h = it >> 4, q16 = it & 15;
-        const float inv = s_inv[h];
-        float acc[16];
+    // pass 2: groups of hg heads, all sr partials' rows of the group per load
+    const int hg = max(1, min(H, (int)(kMergeDataBytes / (1024u * (uint32_t)sr))));
+    const uint32_t bar = bar_addr(c, BAR_MERGE);
+    for (int h0 = 0; h0 < H; h0 += hg) {
+        const int nh = min(hg, H - h0);
+        if (tid == 0) {
+            asm volatile("fence.proxy.async.global;" ::: "memory");  // partials were written by the generic proxy
+            mbar_expect_tx(bar, (uint32_t)(sr * nh) * 1024u);
+            for (int i = 0; i < sr; ++i)
+                bulk_g2s(c.sb + (uint32_t)(i * nh) * 1024u,
+                         p.po + ((size_t)(d.row_u0 + i) * 2 + c.half) * H * 256 + (size_t)h0 * 256,
+                         (uint32_t)nh * 1024u, bar);
+        }
+        // bounded wait; on a timeout the group is skipped (the error word says so)
+        const bool ok = mbar_wait_bounded<false>(bar, merge_phase, kWaitNs);
+        merge_phase ^= 1u;
+        if (!ok) { *c.abort = 1u; break; }
+        // item = (head, 8 dims): thread reads 32 B of each partial row
+        const float* data = reinterpret_cast<const float*>(smem);
+        for (int it = tid; it < nh * 32; it += kThreads) {
+            const int hl = it >> 5, q = it & 31, h = h0 + hl;
+            const float inv = s_inv[h];
+            float acc[8];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) acc[j] = 0.f;
-#pragma unroll 1
-        for (int i = 0; i < sr; i += 4) {
-            float4 v[4][4];
-            float w[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int ii = min(i + k, sr - 1);
-                const float* src = p.po + ((size_t)(d.row_u0 + ii) * H + h) * SMLA_HEAD_DIM + 256 * c.half + 16 * q16;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) v[k][q] = __ldcg(reinterpret_cast<const float4*>(src + 4 * q));
-                w[k] = (i + k < sr) ? s_w[ii * H + h] : -1.f;
-            }
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const bool use = w[k] >= 0.f;
-                const float wk = use ? w[k] * inv : 0.f;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    acc[4 * q] = use ? acc[4 * q] + wk * v[k][q].x : acc[4 * q];
-                    acc[4 * q + 1] = use ? acc[4 * q + 1] + wk * v[k][q].y : acc[4 * q + 1];
-                    acc[4 * q + 2] = use ? acc[4 * q + 2] + wk * v[k][q].z : acc[4 * q + 2];
-                    acc[4 * q + 3] = use ? acc[4 * q + 3] + wk * v[k][q].w : acc[4 * q + 3];
+            for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+            for (int i = 0; i < sr; ++i) {
+                const float w = s_w[i * H + h];
+                const float4 x0 = *reinterpret_cast<const float4*>(data + ((size_t)(i * nh + hl) * 256 + 8 * q));
+                const float4 x1 = *reinterpret_cast<const float4*>(data + ((size_t)(i * nh + hl) * 256 + 8 * q + 4));
+                if (w >= 0.f) {
+                    const float wk = w * inv;
+                    acc[0] += wk * x0.x; acc[1] += wk * x0.y; acc[2] += wk * x0.z; acc[3] += wk * x0.w;
+                    acc[4] += wk * x1.x; acc[5] += wk * x1.y; acc[6] += wk * x1.z; acc[7] += wk * x1.w;
                 }
             }
+            uint4 o;
+            o.x = pack_bf16(acc[0], acc[1]); o.y = pack_bf16(acc[2], acc[3]);
+            o.z = pack_bf16(acc[4], acc[5]); o.w = pack_bf16(acc[6], acc[7]);
+            *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + ((size_t)r * H + h) * SMLA_HEAD_DIM + 256 * c.half + 8 * q) = o;
         }
-        uint16_t* outp = static_cast<uint16_t*>(a.out) + ((size_t)r * H + h) * SMLA_HEAD_DIM + 256 * c.half + 16 * q16;
-        uint4 w0, w1;
-        w0.x = pack_bf16(acc[0], acc[1]); w0.y = pack_bf16(acc[2], acc[3]);
-        w0.z = pack_bf16(acc[4], acc[5]); w0.w = pack_bf16(acc[6], acc[7]);
-        w1.x = pack_bf16(acc[8], acc[9]); w1.y = pack_bf16(acc[10], acc[11]);
-        w1.z = pack_bf16(acc[12], acc[13]); w1.w = pack_bf16(acc[14], acc[15]);
-        reinterpret_cast<uint4*>(outp)[0] = w0;
-        reinterpret_cast<uint4*>(outp)[1] = w1;
+        __syncthreads();  // the data area is refilled by the next group
     }
-    __syncthreads();
     if (tid == 0) atomicExch(p.counters + 2 * r + c.half, 0u);
 }
 
@@ -1153,6 +1166,7 @@ __global__ void __launch_bounds__(kThreads, 1) smla_decode_kernel(const KParams 
         mbar_init(bar_addr(c, BAR_O_DONE), 1);
         mbar_init(bar_addr(c, BAR_Q_READY), kSoftmaxWarps);
         mbar_init(bar_addr(c, BAR_MMA_FINAL), 1);
+        mbar_init(bar_addr(c, BAR_MERGE), 1);
         fence_mbar_init_cluster();
     }
     if (warp == kMmaWarp) {
@@ -1337,12 +1351,12 @@ __global__ void __launch_bounds__(kThreads, 1) smla_decode_kernel(const KParams 
     // Merges this CTA owes (it arrived last at those rows), with every warp;
     // the pipeline's shared memory is free now and holds the weights.
     if (*c.abort == 0u) {
-        float* s_w = reinterpret_cast<float*>(smem + kOffXO);    // [s_r][H] partial weights (own + peer stages)
-        float* s_inv = reinterpret_cast<float*>(smem + kOffRaw);  // [H] 1 / Z (raw ring)
+        uint32_t merge_phase = 0;
         for (int ui = 0; ui < n_units; ++ui) {
             if (units[ui].pad0 == 0) continue;
             __threadfence();
-            merge_row(p, c, units[ui], s_w, s_inv);
+            merge_row(p, c, units[ui], merge_phase);
+            if (*c.abort) break;
         }
     }
     if (err != 0u) atomicOr(p.err, err);

@@ -14,7 +14,7 @@ struct WorkspaceLayout {
     size_t off_err;       // uint32 device error word
     size_t off_counters;  // uint32 [SMLA_MAX_ROWS][2] arrival counters (row, dim half)
     size_t off_ml;        // float2 [units][2][H]  per-unit (m, l), one copy per dim half
-    size_t off_po;        // float  [units][H][512] per-unit unnormalised O (units = unit_capacity)
+    size_t off_po;        // float  [units][2][H][256] per-unit unnormalised O by dims half (units = unit_capacity)
     size_t total;
 };
 
