@@ -82,6 +82,7 @@ constexpr int kMaxUnitsPerPair = 32;
 constexpr int kUnitCostTiles = 2;     // plan estimate: staging + finishing a unit, in tiles
 constexpr int kMinStreamTiles = 4;    // a stream-plan range is at least this many tiles
 constexpr int kMaxStreamRanges = 96;  // stream-plan ranges (pairs) at most: bounds a row's partials
+constexpr int kPlanWarp = 1;          // computes the split plan during setup
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;        // O half: columns [0, 256)
@@ -1080,34 +1081,6 @@ __device__ void merge_row(const KParams& p, const Ctx& c, const UnitDesc& d, uin
 // ---------------------------------------------------------------------------
 // plan helpers (prologue, all threads of the CTA)
 // ---------------------------------------------------------------------------
-// out[r] = sum of f(r') for r' < r, r < R, and out[R] = the total.  Thread t
-// takes a contiguous block of rows; `red` is CTA scratch of kWarps entries.
-template <class F>
-__device__ void block_exclusive_scan(int R, const int* /*unused*/, int* out, long long* red, F f) {
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int per = (R + kThreads - 1) / kThreads;
-    int my_sum = 0;
-    for (int r = tid * per; r < min(R, (tid + 1) * per); ++r) my_sum += f(r);
-    int incl = my_sum;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-    }
-    __syncthreads();
-    if (lane == 31) red[warp] = incl;
-    __syncthreads();
-    int base = 0;
-    for (int w = 0; w < warp; ++w) base += (int)red[w];
-    int run = base + incl - my_sum;
-    for (int r = tid * per; r < min(R, (tid + 1) * per); ++r) {
-        out[r] = run;
-        run += f(r);
-    }
-    if (tid == kThreads - 1) out[R] = run;
-    __syncthreads();
-}
-
 // The row holding tile position pos of the concatenated stream (the last r
 // with cum[r] <= pos; rows with no tile are skipped over by cum).
 __device__ __forceinline__ int row_of_tile(const int* cum, int R, long long pos) {
@@ -1119,107 +1092,83 @@ __device__ __forceinline__ int row_of_tile(const int* cum, int R, long long pos)
     return lo;
 }
 
-// The stream range q (of Q equal ranges [q T / Q, (q + 1) T / Q)) holding pos.
+// The stream range q (of Q equal ranges [q T / Q, (q + 1) T / Q)) holding pos,
+// and the start of range q.  32-bit division when T * Q fits (64-bit integer
+// division is a long software sequence).
 __device__ __forceinline__ int stream_range_of(long long pos, long long T, int Q) {
+    if (T * Q < (1LL << 32)) return (int)(((uint32_t)(pos + 1) * (uint32_t)Q - 1u) / (uint32_t)T);
     return (int)(((pos + 1) * Q - 1) / T);
 }
+__device__ __forceinline__ long long stream_range_start(int q, long long T, int Q) {
+    if (T * Q < (1LL << 32)) return (long long)(((uint32_t)q * (uint32_t)T) / (uint32_t)Q);
+    return (long long)q * T / Q;
+}
 
-// ---------------------------------------------------------------------------
-// the kernel
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads, 1) smla_decode_kernel(const KParams p) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+// out[r] = sum of f(r') for r' < r, r < R, and out[R] = the total; one warp,
+// lane l takes the contiguous rows [l per, (l + 1) per).
+template <class F>
+__device__ void warp_exclusive_scan(int R, int* out, F f) {
+    const int lane = threadIdx.x & 31;
+    const int per = (R + 31) / 32;
+    const int r0 = min(R, lane * per), r1 = min(R, r0 + per);
+    int my_sum = 0;
+    for (int r = r0; r < r1; ++r) my_sum += f(r);
+    int incl = my_sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    int run = incl - my_sum;
+    for (int r = r0; r < r1; ++r) {
+        out[r] = run;
+        run += f(r);
+    }
+    if (lane == 31) out[R] = incl;
+    __syncwarp();
+}
+
+// The split plan, on one warp.  Two candidates, chosen by an estimated
+// makespan in tiles (each unit also costs about kUnitCostTiles of staging and
+// finishing):
+//  (a) chunked: tiles_r per row; smallest chunk c with
+//      sum_r max(1, ceil(tiles_r / c)) <= budget; row r gets
+//      s_r = ceil(tiles_r / ceil(tiles_r / ceil(tiles_r / c))) equal splits and
+//      pair p takes units p, p + n_pairs, ...  The budget is the caller's
+//      rows * num_splits, rounded down to a whole number of passes over the
+//      grid's pairs when it exceeds one pass.
+//  (b) stream: the rows' tiles laid end to end and cut into Q equal ranges,
+//      one per pair; a row crossing a cut gets one unit per range it meets
+//      (at most rows + Q - 1 units, which the workspace always holds).  Rows
+//      with no tile get one empty unit each, on pair r % Q.
+// Writes this pair's unit list and its length (misc[2]).
+__device__ void plan_warp(const KParams& p, int pair, int n_pairs, UnitDesc* units, volatile uint32_t* misc,
+                          int* s_tiles, int* s_prefix, int* s_cum, uint32_t& plan_err) {
     const smla_decode_args& a = p.a;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    Ctx c;
-    c.sb = smem_addr(smem);
-    c.half = blockIdx.x & 1u;
-    volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + kOffMisc);
-    c.abort = misc + 1;
-    long long* red = reinterpret_cast<long long*>(smem + kOffMisc + 64);
-    int* s_tiles = reinterpret_cast<int*>(smem + kOffRaw);  // prologue only
-    int* s_prefix = s_tiles + SMLA_MAX_ROWS;                 // [R + 1]
-    int* s_cum = s_prefix + SMLA_MAX_ROWS + 1;               // [R + 1]
-    UnitDesc* units = reinterpret_cast<UnitDesc*>(smem + kOffUnits);
+    const int lane = threadIdx.x & 31;
     const int R = a.num_rows;
-    const int pair = blockIdx.x >> 1;
-    const int n_pairs = gridDim.x >> 1;
-
-    uint32_t err = 0;
-    if (tid == 0) {
-        misc[1] = 0u;
-        for (int i = 0; i < kNR; ++i) {
-            mbar_init(bar_addr(c, BAR_RAW_FULL + i), 33);  // 32 async (cp.async) + 1 (producer lane 0)
-            mbar_init(bar_addr(c, BAR_RAW_EMPTY + i), kNumDequantWarps);
-        }
-        for (int i = 0; i < kNXO; ++i) {
-            mbar_init(bar_addr(c, BAR_X_FULL + i), kNumDequantWarps);
-            mbar_init(bar_addr(c, BAR_XO_EMPTY + i), 1);
-        }
-        mbar_init(bar_addr(c, BAR_XP_EMPTY), 1);
-        mbar_init(bar_addr(c, BAR_XP_FULL), kNumDequantWarps);
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(bar_addr(c, BAR_S_FULL + i), 1);
-            mbar_init(bar_addr(c, BAR_P_FULL + i), kSoftmaxWarps);
-        }
-        mbar_init(bar_addr(c, BAR_O_DONE), 1);
-        mbar_init(bar_addr(c, BAR_Q_READY), kSoftmaxWarps);
-        mbar_init(bar_addr(c, BAR_MMA_FINAL), 1);
-        mbar_init(bar_addr(c, BAR_MERGE), 1);
-        fence_mbar_init_cluster();
-    }
-    if (warp == kMmaWarp) {
-        tmem_alloc(c.sb + kOffMisc, kTmemCols);
-        tmem_relinquish();
-    }
-
-    // ---- in-kernel split plan (identical in every CTA; reads live lengths) ----
-    // Two candidates, chosen by an estimated makespan in tiles (each unit also
-    // costs about kUnitCostTiles of staging and finishing):
-    //  (a) chunked: tiles_r per row; smallest chunk c with
-    //      sum_r max(1, ceil(tiles_r / c)) <= budget; row r gets
-    //      s_r = ceil(tiles_r / ceil(tiles_r / ceil(tiles_r / c))) equal splits and
-    //      pair p takes units p, p + n_pairs, ...  The budget is the caller's
-    //      rows * num_splits, rounded down to a whole number of passes over the
-    //      grid's pairs when it exceeds one pass.
-    //  (b) stream: the rows' tiles laid end to end and cut into Q equal ranges,
-    //      one per pair; a row crossing a cut gets one unit per range it meets
-    //      (at most rows + Q - 1 units, which the workspace always holds).  Rows
-    //      with no tile get one empty unit each, on pair r % Q.
     const int budget = max(R, p.units > n_pairs ? (p.units / n_pairs) * n_pairs : p.units);
-    uint32_t plan_err = 0;
-    int local_max = 0;
-    for (int r = tid; r < R; r += kThreads) {
+    int max_t = 1;
+    for (int r = lane; r < R; r += 32) {
         const int t = row_tiles(a, r, plan_err);
         s_tiles[r] = t;
-        local_max = max(local_max, t);
+        max_t = max(max_t, t);
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) local_max = max(local_max, __shfl_xor_sync(0xffffffffu, local_max, o));
-    __syncthreads();
-    if (lane == 0) red[16 + warp] = local_max;
-    __syncthreads();
-    int max_t = 1;
-    for (int w = 0; w < kWarps; ++w) max_t = max(max_t, (int)red[16 + w]);
+    for (int o = 16; o > 0; o >>= 1) max_t = max(max_t, __shfl_xor_sync(0xffffffffu, max_t, o));
+    __syncwarp();
     int lo = 1, hi = max_t;
     while (lo < hi) {
         const int mid = (lo + hi) >> 1;
         long long cnt = 0;
-        for (int r = tid; r < R; r += kThreads) cnt += max(1, ceil_div_i(s_tiles[r], mid));
+        for (int r = lane; r < R; r += 32) cnt += max(1, ceil_div_i(s_tiles[r], mid));
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
-        __syncthreads();
-        if (lane == 0) red[warp] = cnt;
-        __syncthreads();
-        long long tot = 0;
-        for (int w = 0; w < kWarps; ++w) tot += red[w];
-        if (tot <= budget) hi = mid; else lo = mid + 1;
+        if (cnt <= budget) hi = mid; else lo = mid + 1;
     }
     const int chunk = lo;
-    // exclusive scans over rows: s_cum (tiles) and s_prefix (chunked units)
-    block_exclusive_scan(R, s_tiles, s_cum, red, [&](int r) { return s_tiles[r]; });
-    block_exclusive_scan(R, s_tiles, s_prefix, red, [&](int r) {
+    warp_exclusive_scan(R, s_cum, [&](int r) { return s_tiles[r]; });
+    warp_exclusive_scan(R, s_prefix, [&](int r) {
         const int t = s_tiles[r];
         int sr = max(1, ceil_div_i(t, chunk));
         if (t > 0) sr = ceil_div_i(t, ceil_div_i(t, sr));
@@ -1234,9 +1183,9 @@ __global__ void __launch_bounds__(kThreads, 1) smla_decode_kernel(const KParams 
     if (Q > 1 && T > 0 && Q > min(units_c, n_pairs)) {
         // upper bound on any pair's unit count: rows met by its range + empty rows
         int zero_rows = 0, upp = 0;
-        for (int r = tid; r < R; r += kThreads) zero_rows += s_tiles[r] == 0;
-        for (int q = tid; q < Q; q += kThreads) {
-            const long long ra = q * T / Q, rb = (q + 1) * T / Q;
+        for (int r = lane; r < R; r += 32) zero_rows += s_tiles[r] == 0;
+        for (int q = lane; q < Q; q += 32) {
+            const long long ra = stream_range_start(q, T, Q), rb = stream_range_start(q + 1, T, Q);
             if (ra < rb) upp = max(upp, row_of_tile(s_cum, R, rb - 1) - row_of_tile(s_cum, R, ra) + 1);
         }
 #pragma unroll
@@ -1244,32 +1193,26 @@ __global__ void __launch_bounds__(kThreads, 1) smla_decode_kernel(const KParams 
             zero_rows += __shfl_xor_sync(0xffffffffu, zero_rows, o);
             upp = max(upp, __shfl_xor_sync(0xffffffffu, upp, o));
         }
-        __syncthreads();
-        if (lane == 0) { red[warp] = zero_rows; red[16 + warp] = upp; }
-        __syncthreads();
-        long long zr = 0;
-        int up = 0;
-        for (int w = 0; w < kWarps; ++w) { zr += red[w]; up = max(up, (int)red[16 + w]); }
-        up += (int)min(zr, (long long)((R + Q - 1) / Q));  // empty rows r = q, q + Q, ... of one pair
+        upp += min(zero_rows, (R + Q - 1) / Q);  // empty rows r = q, q + Q, ... of one pair
         const long long passes_c = (units_c + n_pairs - 1) / n_pairs;
         const long long mk_c = (long long)chunk * passes_c + kUnitCostTiles * passes_c;
-        const long long mk_s = (T + Q - 1) / Q + (long long)kUnitCostTiles * up;
-        stream = up <= kMaxUnitsPerPair && mk_s < mk_c;
+        const long long mk_s = (T + Q - 1) / Q + (long long)kUnitCostTiles * upp;
+        stream = upp <= kMaxUnitsPerPair && mk_s < mk_c;
     }
     if (stream) {
         // per-row unit counts of the stream plan, then their prefix (unit ids)
-        block_exclusive_scan(R, s_tiles, s_prefix, red, [&](int r) {
+        warp_exclusive_scan(R, s_prefix, [&](int r) {
             const int t = s_tiles[r];
             if (t == 0) return 1;
             return stream_range_of(s_cum[r + 1] - 1, T, Q) - stream_range_of(s_cum[r], T, Q) + 1;
         });
     }
     const int total_units = s_prefix[R];
-    if (tid == 0) {
+    if (lane == 0) {
         int n = 0;
         if (stream) {
             if (pair < Q) {
-                const long long ra = pair * T / Q, rb = (pair + 1) * T / Q;
+                const long long ra = stream_range_start(pair, T, Q), rb = stream_range_start(pair + 1, T, Q);
                 if (ra < rb) {
                     for (int r = row_of_tile(s_cum, R, ra); r < R && s_cum[r] < rb; ++r) {
                         if (s_tiles[r] == 0) continue;
@@ -1326,6 +1269,60 @@ __global__ void __launch_bounds__(kThreads, 1) smla_decode_kernel(const KParams 
                              (uint32_t)(a.num_heads * SMLA_ROPE_DIMS * 2));
         }
     }
+    __syncwarp();
+}
+
+// ---------------------------------------------------------------------------
+// the kernel
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads, 1) smla_decode_kernel(const KParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    Ctx c;
+    c.sb = smem_addr(smem);
+    c.half = blockIdx.x & 1u;
+    volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + kOffMisc);
+    c.abort = misc + 1;
+    int* s_tiles = reinterpret_cast<int*>(smem + kOffRaw);  // prologue only
+    int* s_prefix = s_tiles + SMLA_MAX_ROWS;                 // [R + 1]
+    int* s_cum = s_prefix + SMLA_MAX_ROWS + 1;               // [R + 1]
+    UnitDesc* units = reinterpret_cast<UnitDesc*>(smem + kOffUnits);
+    const int pair = blockIdx.x >> 1;
+    const int n_pairs = gridDim.x >> 1;
+
+    uint32_t err = 0;
+    if (tid == 0) {
+        misc[1] = 0u;
+        for (int i = 0; i < kNR; ++i) {
+            mbar_init(bar_addr(c, BAR_RAW_FULL + i), 33);  // 32 async (cp.async) + 1 (producer lane 0)
+            mbar_init(bar_addr(c, BAR_RAW_EMPTY + i), kNumDequantWarps);
+        }
+        for (int i = 0; i < kNXO; ++i) {
+            mbar_init(bar_addr(c, BAR_X_FULL + i), kNumDequantWarps);
+            mbar_init(bar_addr(c, BAR_XO_EMPTY + i), 1);
+        }
+        mbar_init(bar_addr(c, BAR_XP_EMPTY), 1);
+        mbar_init(bar_addr(c, BAR_XP_FULL), kNumDequantWarps);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar_addr(c, BAR_S_FULL + i), 1);
+            mbar_init(bar_addr(c, BAR_P_FULL + i), kSoftmaxWarps);
+        }
+        mbar_init(bar_addr(c, BAR_O_DONE), 1);
+        mbar_init(bar_addr(c, BAR_Q_READY), kSoftmaxWarps);
+        mbar_init(bar_addr(c, BAR_MMA_FINAL), 1);
+        mbar_init(bar_addr(c, BAR_MERGE), 1);
+        fence_mbar_init_cluster();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(c.sb + kOffMisc, kTmemCols);
+        tmem_relinquish();
+    }
+
+    // ---- in-kernel split plan (identical in every CTA; reads live lengths),
+    //      computed by one warp while the others set up barriers and TMEM ----
+    uint32_t plan_err = 0;
+    if (warp == kPlanWarp) plan_warp(p, pair, n_pairs, units, misc, s_tiles, s_prefix, s_cum, plan_err);
     if (blockIdx.x == 0 && plan_err) err |= plan_err;
     tc_fence_before();
     __syncthreads();  // barrier inits, TMEM address and unit list visible; plan scratch dead
