@@ -31,8 +31,8 @@
 //                        and the MN-major B of PV) in a 2-stage ring, the other
 //                        256 dims ("peer": QK only) in a single stage that is
 //                        refilled as soon as QK of the previous tile is done;
-//   MMA warp (1 thread)  QK(t): M = 128 heads, N = 64, K = 512 with Q dims
-//                        0..255 from TMEM and 256..511 from shared memory;
+//   MMA warp (1 thread)  QK(t): M = 128 heads, N = 64, K = 512 with Q's peer
+//                        dims from TMEM and its own dims from shared memory;
 //                        then PV(t-1): M = 128, N = 256, K = 64 with P from TMEM;
 //   softmax warps (4)    one thread per head (TMEM lane): online softmax with a
 //                        conditional rescale, P written back over the scores as
@@ -45,7 +45,8 @@
 //                        2^-9; on peaked softmaxes most tiles qualify.
 //
 // TMEM (512 columns): O [0, 256), two score/P buffers [256, 320) and
-// [320, 384), Q dims 0..255 as bf16 pairs [384, 512).  Heads beyond num_heads
+// [320, 384), Q's peer dims (the 256 this CTA does not output) as bf16 pairs
+// [384, 512).  Heads beyond num_heads
 // are zero-padded up to the MMA's M = 128.
 #include <algorithm>
 #include <cstdint>
@@ -87,7 +88,7 @@ constexpr int kPlanWarp = 1;          // computes the split plan during setup
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;        // O half: columns [0, 256)
 constexpr uint32_t kTmemS = 256;      // score / P buffers: [256, 320), [320, 384)
-constexpr uint32_t kTmemQ = 384;      // Q dims 0..255, bf16 packed: [384, 512)
+constexpr uint32_t kTmemQ = 384;      // Q's peer dims, bf16 packed: [384, 512)
 constexpr uint64_t kWaitNs = 2000000000ull;  // bounded-wait limit (2 s)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -102,7 +103,7 @@ constexpr uint32_t kHalfBytes = 4 * kAtomBytes;                 // 256 dims of a
 constexpr uint32_t kRawStageBytes = kRawBK * SMLA_ENTRY_BYTES;  // 18 KB
 
 // Shared-memory layout (offsets from a 1024-byte-aligned base).
-constexpr uint32_t kOffQ = 0;                                      // Q dims 256..511: [4 atoms][128][128 B]
+constexpr uint32_t kOffQ = 0;                                      // Q's own dims: [4 atoms][128][128 B]
 constexpr uint32_t kOffXO = kOffQ + 65536;                         // own dims: [kNXO][4 atoms][64][128 B]
 constexpr uint32_t kOffXP = kOffXO + kNXO * kHalfBytes;            // peer dims: [4 atoms][64][128 B]
 constexpr uint32_t kOffRaw = kOffXP + kHalfBytes;                  // [kNR][32][576 B]
@@ -666,35 +667,27 @@ __device__ void mma_role(const Ctx& c, const UnitDesc* units, int n_units) {
             if (!wait_bar(c, bar_addr(c, BAR_XP_FULL), g & 1u)) { ok = false; break; }
             tc_fence_after();
             const uint64_t xo_desc0 = sdesc_sw128(c.sb + kOffXO + xs * kHalfBytes, 16, 1024);
-            // dims [256 h, 256 h + 256) are in the own buffer, the rest in the peer buffer
-            const uint64_t lo_desc = c.half == 0 ? xo_desc0 : xp_desc0;  // dims 0..255
-            const uint64_t hi_desc = c.half == 0 ? xp_desc0 : xo_desc0;  // dims 256..511
             const uint32_t ts = c.tmem + kTmemS + (g & 1u) * kBK;
             bool pv_issued = false;
-            // The peer dims' K steps go first (the dequant writes them first) and
-            // their completion frees the peer buffer, so the dequant of the next
-            // tile's peer dims overlaps the own dims' K steps.
+            // First the peer dims' 16 K steps (Q from TMEM, X from the peer
+            // buffer): the dequant writes them first, and their completion frees
+            // the peer buffer for the next tile.  Then the own dims' 16 steps (Q
+            // and X from shared memory).
 #pragma unroll 1
             for (int part = 0; part < 2; ++part) {
-                if (part == 1) {
-                    if (!wait_bar(c, bar_addr(c, BAR_X_FULL + xs), (g / kNXO) & 1u)) { ok = false; break; }
-                    tc_fence_after();
-                }
-                const bool lo_dims = (part == 0) == (c.half == 1);  // dims 0..255 are peer dims for half 1
-                const uint32_t acc0 = part == 0 ? 0u : 1u;
-                if (lo_dims) {  // dims 0..255: Q from TMEM
-                    const uint64_t bd0 = lo_desc;
+                if (part == 0) {
 #pragma unroll 4
                     for (int kk = 0; kk < 16; ++kk)
                         mma_bf16_ts(ts, c.tmem + kTmemQ + kk * 8,
-                                    bd0 + (uint64_t)(((kk >> 2) * kAtomBytes + (kk & 3) * 32) >> 4), idesc_qk,
-                                    kk == 0 ? acc0 : 1u);
-                } else {  // dims 256..511: Q from shared memory
+                                    xp_desc0 + (uint64_t)(((kk >> 2) * kAtomBytes + (kk & 3) * 32) >> 4), idesc_qk,
+                                    kk == 0 ? 0u : 1u);
+                } else {
+                    if (!wait_bar(c, bar_addr(c, BAR_X_FULL + xs), (g / kNXO) & 1u)) { ok = false; break; }
+                    tc_fence_after();
 #pragma unroll 4
                     for (int kk = 0; kk < 16; ++kk)
                         mma_bf16_ss(ts, q_desc0 + (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4),
-                                    hi_desc + (uint64_t)(((kk >> 2) * kAtomBytes + (kk & 3) * 32) >> 4), idesc_qk,
-                                    kk == 0 ? acc0 : 1u);
+                                    xo_desc0 + (uint64_t)(((kk >> 2) * kAtomBytes + (kk & 3) * 32) >> 4), idesc_qk, 1u);
                 }
                 if (part == 0) {
                     mma_commit(bar_addr(c, BAR_XP_EMPTY));
@@ -752,14 +745,20 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, UnitDesc* units, in
             const size_t hq = (size_t)r * H + (h < H ? h : 0);
             const uint4* qn = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q_nope) + hq * SMLA_NOPE_DIMS);
             const uint4* qr = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q_rope) + hq * SMLA_ROPE_DIMS);
-            // 16 loads in flight per batch: dims 0..255 in two batches
+            // Q in 16-byte chunks j = dims 8j .. 8j + 7 (NoPE chunks 0..55, RoPE 56..63).
+            // The peer dims' 32 chunks go to TMEM (the A operand of QK's first
+            // half), the own dims' 32 to shared memory; 16 loads in flight per batch.
+            const int pbase = 32 * (1 - (int)c.half), obase = 32 * (int)c.half;
 #pragma unroll 1
             for (int bt = 0; bt < 2; ++bt) {
                 uint4 w[16];
 #pragma unroll
-                for (int q = 0; q < 16; ++q) w[q] = h < H ? __ldg(qn + 16 * bt + q) : make_uint4(0u, 0u, 0u, 0u);
+                for (int q = 0; q < 16; ++q) {
+                    const int j = pbase + 16 * bt + q;
+                    w[q] = h >= H ? make_uint4(0u, 0u, 0u, 0u) : (j < 56 ? __ldg(qn + j) : __ldg(qr + (j - 56)));
+                }
 #pragma unroll
-                for (int hc = 0; hc < 2; ++hc) {  // dims 128 bt + 64 hc .. : 32 TMEM columns
+                for (int hc = 0; hc < 2; ++hc) {  // 64 dims -> 32 TMEM columns
                     uint32_t v[32];
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
@@ -769,18 +768,17 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, UnitDesc* units, in
                     tmem_st32(c.tmem + kTmemQ + lane_base + 32 * (2 * bt + hc), v);
                 }
             }
-            // dims 256..511 (NoPE 256..447, then RoPE 0..63): 16-byte chunk k = 8 dims
 #pragma unroll 1
             for (int bt = 0; bt < 2; ++bt) {
                 uint4 w[16];
 #pragma unroll
                 for (int q = 0; q < 16; ++q) {
-                    const int k = 16 * bt + q;
-                    w[q] = h >= H ? make_uint4(0u, 0u, 0u, 0u) : (k < 24 ? __ldg(qn + 32 + k) : __ldg(qr + (k - 24)));
+                    const int j = obase + 16 * bt + q;
+                    w[q] = h >= H ? make_uint4(0u, 0u, 0u, 0u) : (j < 56 ? __ldg(qn + j) : __ldg(qr + (j - 56)));
                 }
 #pragma unroll
                 for (int q = 0; q < 16; ++q) {
-                    const int k = 16 * bt + q;
+                    const int k = 16 * bt + q;  // own chunk k: atom k / 8, 16-byte column k % 8
                     st_shared_v4(c.sb + kOffQ + (k >> 3) * 16384 + sw128_offset(h, k & 7), w[q].x, w[q].y, w[q].z, w[q].w);
                 }
             }
