@@ -90,11 +90,17 @@ def load_peaks():
 
 
 def kernel_source_hash():
+    """Hash of the device sources' code: comments and whitespace are left out,
+    so that only a change to the compiled kernel makes recorded counters stale."""
     h = hashlib.sha256()
     for fn in sorted(os.listdir(os.path.dirname(KERNEL_SRC))):
         if fn.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(os.path.dirname(KERNEL_SRC), fn), "rb") as f:
-                h.update(f.read())
+            with open(os.path.join(os.path.dirname(KERNEL_SRC), fn)) as f:
+                src = f.read()
+            src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+            src = re.sub(r"//[^\n]*", " ", src)
+            h.update(fn.encode())
+            h.update(" ".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -731,9 +731,10 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, UnitDesc* units, in
         const UnitDesc d = units[ui];
         const int r = d.row;
         const int n = d.t_end - d.t_begin;
-        // ---- Q of this row: dims 0..255 -> TMEM [384, 512) as bf16 pairs,
-        //      dims 256..511 -> shared memory, K-major with the 128-byte swizzle.
-        //      The next unit's q rows are prefetched into L2 now, a unit ahead.
+        // ---- Q of this row: its peer dims (the 256 this CTA does not output)
+        //      -> TMEM [384, 512) as bf16 pairs, its own dims -> shared memory,
+        //      K-major with the 128-byte swizzle.  The next unit's q rows are
+        //      prefetched into L2 now, a unit ahead.
         {
             if (h == 0 && ui + 1 < n_units) {
                 const size_t rn = (size_t)units[ui + 1].row * H;
