@@ -5,8 +5,9 @@ A step is one decode call over one batch: the DeepSeek-V4-like decode
 workload (32 rows x 128 heads, 32K context in 64-token pages, top-k 2048
 with 2% invalid slots, window 128, 8192 compressed entries per row) by
 default.  Inputs are resident in HBM; L2 is flushed (a 512 MB write) before
-every timed step; each step replays a CUDA graph holding the one decode
-launch and is timed with CUDA events on that stream.
+every timed step; each step replays a CUDA graph holding the call's two
+launches (the decode kernel, then the merge kernel for split rows) and is
+timed with CUDA events on that stream.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
@@ -34,6 +35,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "sparse-MLA decode µs/call & query-rows/s; % of HBM/tensor roofline, 1×GB300"
 KERNEL_NAME = "smla_decode_kernel"
+LAUNCHES_PER_CALL = 2  # smla_decode enqueues the decode kernel and the merge kernel
 KERNEL_SRC = os.path.join(ROOT, "sparse_mla_decode_04_gb300", "csrc", "smla_decode.cu")
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -383,10 +385,11 @@ def run_gpu(args):
                      "traffic": traffic, "peak_source": f"{peak_src} (MEASURED_PEAKS.json burst)"
                      if peak_src == "measured" else "fallback",
                      "algorithmic_bytes": nbytes, "algorithmic_flops": flops,
-                     "t_roofline_us": max(t_tc, t_hbm) * 1e6, "kernel": KERNEL_NAME},
+                     "t_roofline_us": max(t_tc, t_hbm) * 1e6,
+                     "kernel": f"{KERNEL_NAME} (timed with smla_merge_kernel: the whole call)"},
         "e2e": {"value": rows_total / (e2e_step / 1e3), "unit": "query-rows/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_step},
-        "gpu_launches": args.steps,
+        "gpu_launches": LAUNCHES_PER_CALL * args.steps,
         "clocks": clocks.summary(),
         "wall_s_timed_region": t_wall,
     }

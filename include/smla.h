@@ -21,11 +21,13 @@
  * zero probability, 64-bit block address arithmetic; and "[ASM] [HIP] [MLA v4
  * nm] Split plan helper and persistent decode kernel with in-kernel split and
  * merge" (ROCm/aiter pull request 6126), summary part 1 (host split planner
- * from a cost model) and part 2 (one launch; split plan computed in the
- * kernel from the real lengths on every call; split rows merged by the
- * last-arriving work-group from fp32 partials plus LSE; unsplit rows write
- * bf16 directly; CUDA-graph safe with varying lengths; the workspace is
- * allocated outside capture and calls sharing it are stream-ordered).
+ * from a cost model) and part 2 (split plan computed in the kernel from the
+ * real lengths on every call; split rows merged from fp32 partials plus LSE;
+ * unsplit rows write bf16 directly; CUDA-graph safe with varying lengths; the
+ * workspace is allocated outside capture and calls sharing it are
+ * stream-ordered).  There the last-arriving work-group of a row merges it
+ * inside the one launch; here a second launch merges every split row at once
+ * across the whole GPU, which keeps the merge off the decode kernel's tail.
  *
  * Threading: every function is thread-safe.  The library allocates no device
  * memory and keeps no per-call state; the caller owns every buffer.
@@ -60,7 +62,7 @@ typedef enum smla_status {
 #define SMLA_DEV_BAD_CMP     0x2u  /* compressed range outside [0, n_cmp): the excess is dropped */
 #define SMLA_DEV_BAD_LENGTH  0x4u  /* negative swa_len / cmp_len: treated as 0 */
 #define SMLA_DEV_TIMEOUT     0x8u  /* a bounded wait inside the kernel gave up; outputs of the
-                                      call are undefined and the workspace must be re-zeroed */
+                                      call are undefined */
 
 /* Fixed geometry of one KV entry. */
 #define SMLA_NOPE_DIMS   448
@@ -149,20 +151,23 @@ int smla_plan_num_splits_ex(int num_rows, int num_heads, int64_t kv_len,
  * Workspace bytes for calls with up to max_rows rows, num_heads heads and a
  * split budget of max_splits (cf. the persistent kernel's workspace getter in
  * aiter pull request 6126, summary part 2).  The layout is: a device error
- * word, per-(row, half) arrival counters, per-unit fp32 partial (m, l) and
- * per-unit fp32 partial O, for max(max_rows * max_splits, max_rows + 95)
- * units (the second term lets the stream plan use up to 96 CTA pairs).
- * Allocate it once, zero it once (cudaMemset 0),
- * outside any graph capture; every successful call leaves the counters back
- * at zero, so it can be reused across calls and batch sizes.  Returns 0 for
- * arguments out of range.
+ * word, a per-row table of partials (rewritten by every call), per-unit fp32
+ * partial (m, l) and per-unit fp32 partial O, for
+ * max(max_rows * max_splits, max_rows + 95) units (the second term lets the
+ * stream plan use up to 96 CTA pairs).  Allocate it once and zero it once
+ * (cudaMemset 0, for the error word), outside any graph capture; it carries
+ * no other state between calls, so it can be reused across calls and batch
+ * sizes.  Returns 0 for arguments out of range.
  */
 size_t smla_workspace_bytes(int max_rows, int num_heads, int max_splits);
 
 /*
- * One decode step: validates on the host, then enqueues ONE kernel launch on
- * `stream`: a persistent grid of CTA pairs (one CTA per output dim half), as
- * many as are co-resident on the device.
+ * One decode step: validates on the host, then enqueues two kernel launches
+ * on `stream`: the decode kernel, a persistent grid of CTA pairs (one CTA per
+ * output dim half, as many as are co-resident on the device), which writes
+ * unsplit rows' out and lse and split rows' fp32 partials; then the merge
+ * kernel, one block per (row, dim half, 8 heads), which combines the partials
+ * of split rows.
  * Host checks come first: NULL or misaligned pointers, unsupported sizes, a
  * workspace smaller than smla_workspace_bytes(num_rows, num_heads, num_splits)
  * and a device that is not sm_103 each return an error and launch nothing.
@@ -170,7 +175,7 @@ size_t smla_workspace_bytes(int max_rows, int num_heads, int max_splits);
  * device data sets bits in the workspace error word (SMLA_DEV_*) and never
  * traps.  Rows with no valid entry get out = 0 and lse = sink (written).
  * Calls that share a workspace must be ordered on one stream.
- * Returns SMLA_OK once the launch is enqueued.
+ * Returns SMLA_OK once both launches are enqueued.
  */
 smla_status smla_decode(const smla_decode_args* args, void* workspace, size_t ws_bytes,
                         smla_stream_t stream);
@@ -208,7 +213,7 @@ const char* smla_status_string(smla_status status);
  *   (cudaGetSymbolAddress, with that device current) and caches it; make that
  *   first call before any stream capture on the device.
  * - Every call on a device shares the one array, and the array keeps what the
- *   last call left.  Each call clears the error word and arrival counters on
+ *   last call left.  Each call clears the error word (and the row table) on
  *   `stream` before its launch, so the SMLA_DEV_* flags of a call cannot be
  *   read back through this entry point.  Calls that overlap on the GPU (other
  *   streams, other host threads) race on the array: order them on one stream.

@@ -5,9 +5,9 @@
 // dims) against the entries the row selects (top-k main-cache slots with -1 as
 // an invalid slot, a sliding window, compressed-cache 64-entry groups with a
 // masked tail), a softmax with a per-head sink logit, and a 512-wide PV.
-// Split plan, last-arriver merge and graph safety follow "[ASM] [HIP] [MLA v4
+// Split plan, merge of split rows and graph safety follow "[ASM] [HIP] [MLA v4
 // nm] Split plan helper and persistent decode kernel with in-kernel split and
-// merge", summary part 2.
+// merge", summary part 2 (here the merge is a second, GPU-wide kernel).
 //
 // GB300 design.  A work unit is (row, split).  O for 128 heads x 512 dims in
 // fp32 would fill a whole SM's TMEM, so each unit runs on two CTAs and CTA c
@@ -120,7 +120,6 @@ constexpr uint32_t kOffUnits = kOffMisc + kMiscBytes;           // unit descript
 constexpr uint32_t kSmemUsed = kOffUnits + kMaxUnitsPerPair * 32;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;               // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-// merge weights [s_r][H] fit in the own + peer stages for any s_r the plans make
 // The plan's per-row scratch (tiles[R], prefix[R+1]) aliases the raw ring
 // during the prologue, before any producer runs.
 static_assert(4 * (3 * SMLA_MAX_ROWS + 8) <= kNR * kRawStageBytes, "plan scratch fits in the raw ring");
@@ -138,15 +137,14 @@ enum : uint32_t {
     BAR_O_DONE = BAR_P_FULL + 2,           // MMA commit after each PV
     BAR_Q_READY = BAR_O_DONE + 1,          // softmax -> MMA, once per unit (kSoftmaxWarps)
     BAR_MMA_FINAL = BAR_Q_READY + 1,       // teardown: all MMAs retired
-    BAR_MERGE = BAR_MMA_FINAL + 1,         // final merges: partials loaded (1 arrival + tx bytes)
-    BAR_COUNT = BAR_MERGE + 1
+    BAR_COUNT = BAR_MMA_FINAL + 1
 };
 static_assert(BAR_COUNT <= kNumBars, "barrier slots");
 
 struct KParams {
     smla_decode_args a;
     uint32_t* err;
-    uint32_t* counters;  // [SMLA_MAX_ROWS][2]
+    int2* row_table;     // [SMLA_MAX_ROWS] (first unit, partials) per row: block 0's plan -> merge kernel
     float2* ml;          // [units][2][H]   (m in log2 units, l)
     float* po;           // [units][2][H][256] unnormalised fp32 O, by dims half
     int units;           // num_rows * num_splits: the chunked plan's unit budget
@@ -155,8 +153,7 @@ struct KParams {
 
 struct UnitDesc {
     int row, s_r, row_u0, unit, t_begin, t_end;
-    int pad0;  // set to 1 when this CTA arrived last at the unit's row and owes its merge
-    int pad1;
+    int pad0, pad1;
 };
 
 // ---------------------------------------------------------------------------
@@ -711,6 +708,32 @@ __device__ void mma_role(const Ctx& c, const UnitDesc* units, int n_units) {
 }
 
 // ---------------------------------------------------------------------------
+// finish stores through shared memory
+// ---------------------------------------------------------------------------
+// A unit's result leaves TMEM one row per thread (thread = head); stored
+// straight to global memory, each 16-byte store of a warp would touch 32 rows.
+// Instead each warp stages its 32 rows of 512 bytes in the Q region (free
+// between the unit's last QK and the next unit's Q staging) and writes them
+// out one row per instruction, 512 contiguous bytes per warp store.  Row h
+// sits at Q + 512 h with its 16-byte chunks XOR-swizzled by h % 32, so both
+// the row-wise stores and the column-wise loads stay free of bank conflicts.
+__device__ __forceinline__ uint32_t stage_addr(const Ctx& c, int h, int chunk) {
+    return c.sb + kOffQ + (uint32_t)h * 512u + (uint32_t)((chunk ^ (h & 31)) * 16);
+}
+// Write this warp's 32 staged rows: row h (h < H) to dst_row(h) (512 bytes).
+template <class RowPtr>
+__device__ __forceinline__ void stage_flush(const Ctx& c, int warp, int lane, int H, RowPtr dst_row) {
+    __syncwarp();
+#pragma unroll 4
+    for (int rr = 0; rr < 32; ++rr) {
+        const int h = 32 * warp + rr;
+        const uint4 v = ld_shared_v4(stage_addr(c, h, lane));
+        if (h < H) __stcg(reinterpret_cast<uint4*>(dst_row(h)) + lane, v);
+    }
+    __syncwarp();
+}
+
+// ---------------------------------------------------------------------------
 // role: softmax / epilogue (warps 0-3, thread = head = TMEM lane)
 // ---------------------------------------------------------------------------
 __device__ void softmax_role(const KParams& p, const Ctx& c, UnitDesc* units, int n_units, uint32_t& err) {
@@ -722,8 +745,6 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, UnitDesc* units, in
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     const float qscale = a.sm_scale * kLog2e;
     const float sink2 = (a.sink != nullptr && h < H) ? __ldg(a.sink + h) * kLog2e : -INFINITY;
-    volatile uint32_t* flag = reinterpret_cast<volatile uint32_t*>(
-        static_cast<uint8_t*>(__cvta_shared_to_generic(c.sb + kOffMisc + 12)));  // misc[3]
     uint32_t g = 0, pv = 0;
     bool ok = true;
 
@@ -743,44 +764,50 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, UnitDesc* units, in
                 bulk_prefetch_l2(static_cast<const uint16_t*>(a.q_rope) + rn * SMLA_ROPE_DIMS,
                                  (uint32_t)(H * SMLA_ROPE_DIMS * 2));
             }
-            const size_t hq = (size_t)r * H + (h < H ? h : 0);
-            const uint4* qn = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q_nope) + hq * SMLA_NOPE_DIMS);
-            const uint4* qr = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.q_rope) + hq * SMLA_ROPE_DIMS);
-            // Q in 16-byte chunks j = dims 8j .. 8j + 7 (NoPE chunks 0..55, RoPE 56..63).
-            // The peer dims' 32 chunks go to TMEM (the A operand of QK's first
-            // half), the own dims' 32 to shared memory; 16 loads in flight per batch.
+            // Q in 16-byte chunks j = dims 8j .. 8j + 7 (NoPE chunks 0..55, RoPE
+            // 56..63).  Each warp reads its 32 heads one head per load
+            // instruction (lane = chunk: coalesced), 8 loads in flight.  The
+            // peer dims' 32 chunks go to TMEM (the A operand of QK's first half)
+            // through a row per head staged in the Q region; the own dims' 32
+            // chunks go straight to their place in the Q region, K-major with
+            // the 128-byte swizzle (after every warp has read its staged rows).
+            const uint4* qn = static_cast<const uint4*>(a.q_nope) + (size_t)r * H * (SMLA_NOPE_DIMS / 8);
+            const uint4* qr = static_cast<const uint4*>(a.q_rope) + (size_t)r * H * (SMLA_ROPE_DIMS / 8);
             const int pbase = 32 * (1 - (int)c.half), obase = 32 * (int)c.half;
 #pragma unroll 1
-            for (int bt = 0; bt < 2; ++bt) {
-                uint4 w[16];
-#pragma unroll
-                for (int q = 0; q < 16; ++q) {
-                    const int j = pbase + 16 * bt + q;
-                    w[q] = h >= H ? make_uint4(0u, 0u, 0u, 0u) : (j < 56 ? __ldg(qn + j) : __ldg(qr + (j - 56)));
-                }
-#pragma unroll
-                for (int hc = 0; hc < 2; ++hc) {  // 64 dims -> 32 TMEM columns
-                    uint32_t v[32];
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        v[4 * q] = w[8 * hc + q].x; v[4 * q + 1] = w[8 * hc + q].y;
-                        v[4 * q + 2] = w[8 * hc + q].z; v[4 * q + 3] = w[8 * hc + q].w;
-                    }
-                    tmem_st32(c.tmem + kTmemQ + lane_base + 32 * (2 * bt + hc), v);
-                }
-            }
+            for (int pass = 0; pass < 2; ++pass) {
+                const int j = (pass == 0 ? pbase : obase) + lane;
 #pragma unroll 1
-            for (int bt = 0; bt < 2; ++bt) {
-                uint4 w[16];
+                for (int r0 = 0; r0 < 32; r0 += 8) {
+                    uint4 w[8];
 #pragma unroll
-                for (int q = 0; q < 16; ++q) {
-                    const int j = obase + 16 * bt + q;
-                    w[q] = h >= H ? make_uint4(0u, 0u, 0u, 0u) : (j < 56 ? __ldg(qn + j) : __ldg(qr + (j - 56)));
+                    for (int k = 0; k < 8; ++k) {
+                        const int hh = 32 * warp + r0 + k;
+                        w[k] = hh >= H ? make_uint4(0u, 0u, 0u, 0u)
+                                       : (j < 56 ? __ldg(qn + (size_t)hh * (SMLA_NOPE_DIMS / 8) + j)
+                                                 : __ldg(qr + (size_t)hh * (SMLA_ROPE_DIMS / 8) + (j - 56)));
+                    }
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const int hh = 32 * warp + r0 + k;
+                        const uint32_t dst = pass == 0 ? stage_addr(c, hh, lane)
+                                                       : c.sb + kOffQ + (lane >> 3) * 16384 + sw128_offset(hh, lane & 7);
+                        st_shared_v4(dst, w[k].x, w[k].y, w[k].z, w[k].w);
+                    }
                 }
+                if (pass == 0) {
+                    __syncwarp();
+#pragma unroll 1
+                    for (int hc = 0; hc < 4; ++hc) {  // 64 dims -> 32 TMEM columns
+                        uint32_t v[32];
 #pragma unroll
-                for (int q = 0; q < 16; ++q) {
-                    const int k = 16 * bt + q;  // own chunk k: atom k / 8, 16-byte column k % 8
-                    st_shared_v4(c.sb + kOffQ + (k >> 3) * 16384 + sw128_offset(h, k & 7), w[q].x, w[q].y, w[q].z, w[q].w);
+                        for (int q = 0; q < 8; ++q) {
+                            const uint4 w = ld_shared_v4(stage_addr(c, h, 8 * hc + q));
+                            v[4 * q] = w.x; v[4 * q + 1] = w.y; v[4 * q + 2] = w.z; v[4 * q + 3] = w.w;
+                        }
+                        tmem_st32(c.tmem + kTmemQ + lane_base + 32 * hc, v);
+                    }
+                    softmax_bar();  // all staged rows read before the own dims overwrite the region
                 }
             }
             fence_proxy_async_smem();
@@ -911,7 +938,7 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, UnitDesc* units, in
             *c.abort = 1u;
             break;
         }
-        // ---- finish: final bf16 output, or fp32 partial + last-arriver merge ----
+        // ---- finish: final bf16 output, or an fp32 partial for the merge kernel ----
         if (d.s_r == 1) {
             const float M = fmaxf(m_used, sink2);
             float oscale = 0.f, lse = -INFINITY;
@@ -923,7 +950,7 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, UnitDesc* units, in
                 lse = (M + log2f(Z)) * kLn2;
             }
             if (lsum == 0.f) lse = (a.sink != nullptr && h < H) ? __ldg(a.sink + h) : -INFINITY;  // sink only, exactly
-            uint16_t* outp = static_cast<uint16_t*>(a.out) + ((size_t)r * H + (h < H ? h : 0)) * SMLA_HEAD_DIM + 256 * c.half;
+            // 256 bf16 dims per head = one 512-byte staged row
 #pragma unroll 1
             for (int cc = 0; cc < 8; ++cc) {
                 uint32_t v[32];
@@ -934,46 +961,35 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, UnitDesc* units, in
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = 0u;
                 }
-                if (h < H) {
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        uint4 w;
-                        w.x = pack_bf16(__uint_as_float(v[8 * q]) * oscale, __uint_as_float(v[8 * q + 1]) * oscale);
-                        w.y = pack_bf16(__uint_as_float(v[8 * q + 2]) * oscale, __uint_as_float(v[8 * q + 3]) * oscale);
-                        w.z = pack_bf16(__uint_as_float(v[8 * q + 4]) * oscale, __uint_as_float(v[8 * q + 5]) * oscale);
-                        w.w = pack_bf16(__uint_as_float(v[8 * q + 6]) * oscale, __uint_as_float(v[8 * q + 7]) * oscale);
-                        *reinterpret_cast<uint4*>(outp + 32 * cc + 8 * q) = w;
-                    }
-                }
+                for (int q = 0; q < 4; ++q)
+                    st_shared_v4(stage_addr(c, h, 4 * cc + q),
+                                 pack_bf16(__uint_as_float(v[8 * q]) * oscale, __uint_as_float(v[8 * q + 1]) * oscale),
+                                 pack_bf16(__uint_as_float(v[8 * q + 2]) * oscale, __uint_as_float(v[8 * q + 3]) * oscale),
+                                 pack_bf16(__uint_as_float(v[8 * q + 4]) * oscale, __uint_as_float(v[8 * q + 5]) * oscale),
+                                 pack_bf16(__uint_as_float(v[8 * q + 6]) * oscale, __uint_as_float(v[8 * q + 7]) * oscale));
             }
+            stage_flush(c, warp, lane, H, [&](int hh) {
+                return static_cast<uint16_t*>(a.out) + ((size_t)r * H + hh) * SMLA_HEAD_DIM + 256 * c.half;
+            });
             if (c.half == 0 && a.lse != nullptr && h < H) a.lse[(size_t)r * H + h] = lse;
         } else {
             const size_t ub = (size_t)d.unit;
-            float* po = p.po + ((ub * 2 + c.half) * H + (h < H ? h : 0)) * 256;
+            // 256 fp32 dims per head: two passes of 128 dims (one 512-byte staged row)
 #pragma unroll 1
-            for (int cc = 0; cc < 8; ++cc) {
-                uint32_t v[32];
-                tmem_ld32(c.tmem + kTmemO + lane_base + 32 * cc, v);
-                tmem_wait_ld();
-                if (h < H) {
+            for (int hf = 0; hf < 2; ++hf) {
+#pragma unroll 1
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t v[32];
+                    tmem_ld32(c.tmem + kTmemO + lane_base + 128 * hf + 32 * cc, v);
+                    tmem_wait_ld();
 #pragma unroll
                     for (int q = 0; q < 8; ++q)
-                        __stcg(reinterpret_cast<float4*>(po + 32 * cc + 4 * q),
-                               make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                                           __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3])));
+                        st_shared_v4(stage_addr(c, h, 8 * cc + q), v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
                 }
+                stage_flush(c, warp, lane, H, [&](int hh) { return p.po + ((ub * 2 + c.half) * H + hh) * 256 + 128 * hf; });
             }
             if (h < H) __stcg(p.ml + (ub * 2 + c.half) * H + h, make_float2(m_used, lsum));
-            __threadfence();
-            softmax_bar();
-            if (h == 0) {
-                const uint32_t old = atomicAdd(p.counters + 2 * r + c.half, 1u);
-                *flag = (old == (uint32_t)(d.s_r - 1)) ? 1u : 0u;
-            }
-            softmax_bar();
-            // The last arriver merges the row's partials, but only after its
-            // own units are done, with every warp of the CTA (merge_rows).
-            if (h == 0 && *flag != 0u) units[ui].pad0 = 1;
         }
         // All TMEM reads of O are complete (tcgen05.wait::ld) before the next
         // unit's Q is staged; its first PV (which overwrites O) waits for Q.
@@ -981,100 +997,6 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, UnitDesc* units, in
         softmax_bar();
     }
     if (!ok) err |= SMLA_DEV_TIMEOUT;
-}
-
-// ---------------------------------------------------------------------------
-// merge of a split row's partials (this CTA's dims half), run by all threads
-// after the CTA's units are done, when the pipeline's shared memory is free
-// ---------------------------------------------------------------------------
-// Per head: M = max(sink, m_i), Z = sum_i l_i 2^(m_i - M) + 2^(sink - M),
-// out = sum_i 2^(m_i - M) O_i / Z, lse = (M + log2 Z) ln 2, in split order.
-// Partials with m = -inf saw no entry; their O is never used.  The partials'
-// O rows ([half][H][256] per unit, contiguous) come in by bulk copies, a group
-// of heads of every partial at a time.
-constexpr uint32_t kMergeDataBytes = kOffRaw;                 // [0, kOffRaw): partial O rows
-constexpr uint32_t kOffMergeW = kOffRaw;                      // [s_r][H] float weights
-static_assert(kNR * kRawStageBytes >= 4 * SMLA_MAX_HEADS * (96 + 1) + 8 * SMLA_MAX_HEADS, "merge weights fit");
-
-__device__ void merge_row(const KParams& p, const Ctx& c, const UnitDesc& d, uint32_t& merge_phase) {
-    const smla_decode_args& a = p.a;
-    const int H = a.num_heads, tid = threadIdx.x;
-    const int sr = d.s_r, r = d.row;
-    uint8_t* smem = static_cast<uint8_t*>(__cvta_shared_to_generic(c.sb));
-    float* s_w = reinterpret_cast<float*>(smem + kOffMergeW);  // [sr][H]: weight, or -1 for an unused partial
-    float* s_inv = s_w + sr * H;                                // [H]
-    // pass 1a: every (partial, head) m and l into shared memory at once
-    float2* s_ml = reinterpret_cast<float2*>(smem);  // temporary, in the data area
-    for (int k = tid; k < sr * H; k += kThreads) {
-        const int i = k / H, h = k - i * H;
-        s_ml[k] = __ldcg(p.ml + ((size_t)(d.row_u0 + i) * 2 + c.half) * H + h);
-    }
-    __syncthreads();
-    // pass 1b: one thread per head
-    for (int h = tid; h < H; h += kThreads) {
-        const float sink2 = a.sink != nullptr ? __ldg(a.sink + h) * kLog2e : -INFINITY;
-        float M = sink2;
-        for (int i = 0; i < sr; ++i) M = fmaxf(M, s_ml[i * H + h].x);
-        float Z = 0.f, lall = 0.f;
-        if (M != -INFINITY) Z = (sink2 == -INFINITY) ? 0.f : exp2f(sink2 - M);
-        for (int i = 0; i < sr; ++i) {
-            const float2 ml = s_ml[i * H + h];
-            const bool use = ml.x != -INFINITY;
-            if (M != -INFINITY && use) Z += ml.y * exp2f(ml.x - M);
-            lall += ml.y;
-            s_w[i * H + h] = use ? exp2f(ml.x - M) : -1.f;
-        }
-        s_inv[h] = Z > 0.f ? 1.f / Z : 0.f;
-        if (c.half == 0 && a.lse != nullptr) {
-            float lse = (M == -INFINITY || Z <= 0.f) ? -INFINITY : (M + log2f(Z)) * kLn2;
-            if (lall == 0.f) lse = a.sink != nullptr ? __ldg(a.sink + h) : -INFINITY;  // sink only, exactly
-            a.lse[(size_t)r * H + h] = lse;
-        }
-    }
-    __syncthreads();
-    // pass 2: groups of hg heads, all sr partials' rows of the group per load
-    const int hg = max(1, min(H, (int)(kMergeDataBytes / (1024u * (uint32_t)sr))));
-    const uint32_t bar = bar_addr(c, BAR_MERGE);
-    for (int h0 = 0; h0 < H; h0 += hg) {
-        const int nh = min(hg, H - h0);
-        if (tid == 0) {
-            asm volatile("fence.proxy.async.global;" ::: "memory");  // partials were written by the generic proxy
-            mbar_expect_tx(bar, (uint32_t)(sr * nh) * 1024u);
-            for (int i = 0; i < sr; ++i)
-                bulk_g2s(c.sb + (uint32_t)(i * nh) * 1024u,
-                         p.po + ((size_t)(d.row_u0 + i) * 2 + c.half) * H * 256 + (size_t)h0 * 256,
-                         (uint32_t)nh * 1024u, bar);
-        }
-        // bounded wait; on a timeout the group is skipped (the error word says so)
-        const bool ok = mbar_wait_bounded<false>(bar, merge_phase, kWaitNs);
-        merge_phase ^= 1u;
-        if (!ok) { *c.abort = 1u; break; }
-        // item = (head, 8 dims): thread reads 32 B of each partial row
-        const float* data = reinterpret_cast<const float*>(smem);
-        for (int it = tid; it < nh * 32; it += kThreads) {
-            const int hl = it >> 5, q = it & 31, h = h0 + hl;
-            const float inv = s_inv[h];
-            float acc[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) acc[j] = 0.f;
-            for (int i = 0; i < sr; ++i) {
-                const float w = s_w[i * H + h];
-                const float4 x0 = *reinterpret_cast<const float4*>(data + ((size_t)(i * nh + hl) * 256 + 8 * q));
-                const float4 x1 = *reinterpret_cast<const float4*>(data + ((size_t)(i * nh + hl) * 256 + 8 * q + 4));
-                if (w >= 0.f) {
-                    const float wk = w * inv;
-                    acc[0] += wk * x0.x; acc[1] += wk * x0.y; acc[2] += wk * x0.z; acc[3] += wk * x0.w;
-                    acc[4] += wk * x1.x; acc[5] += wk * x1.y; acc[6] += wk * x1.z; acc[7] += wk * x1.w;
-                }
-            }
-            uint4 o;
-            o.x = pack_bf16(acc[0], acc[1]); o.y = pack_bf16(acc[2], acc[3]);
-            o.z = pack_bf16(acc[4], acc[5]); o.w = pack_bf16(acc[6], acc[7]);
-            *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + ((size_t)r * H + h) * SMLA_HEAD_DIM + 256 * c.half + 8 * q) = o;
-        }
-        __syncthreads();  // the data area is refilled by the next group
-    }
-    if (tid == 0) atomicExch(p.counters + 2 * r + c.half, 0u);
 }
 
 // ---------------------------------------------------------------------------
@@ -1207,6 +1129,8 @@ __device__ void plan_warp(const KParams& p, int pair, int n_pairs, UnitDesc* uni
         });
     }
     const int total_units = s_prefix[R];
+    if (blockIdx.x == 0)  // the merge kernel's map of the partials
+        for (int r = lane; r < R; r += 32) p.row_table[r] = make_int2(s_prefix[r], s_prefix[r + 1] - s_prefix[r]);
     if (lane == 0) {
         int n = 0;
         if (stream) {
@@ -1310,12 +1234,22 @@ __global__ void __launch_bounds__(kThreads, 1) smla_decode_kernel(const KParams 
         mbar_init(bar_addr(c, BAR_O_DONE), 1);
         mbar_init(bar_addr(c, BAR_Q_READY), kSoftmaxWarps);
         mbar_init(bar_addr(c, BAR_MMA_FINAL), 1);
-        mbar_init(bar_addr(c, BAR_MERGE), 1);
         fence_mbar_init_cluster();
     }
     if (warp == kMmaWarp) {
         tmem_alloc(c.sb + kOffMisc, kTmemCols);
         tmem_relinquish();
+    }
+    // Start every row's q on its way to L2 while the plan runs (pair p takes
+    // rows p, p + pairs, ...): the first units' Q staging then reads L2.
+    if (warp == kPlanWarp + 1 && lane == 0) {
+        const int H = p.a.num_heads;
+        for (int r = pair; r < p.a.num_rows; r += n_pairs) {
+            bulk_prefetch_l2(static_cast<const uint16_t*>(p.a.q_nope) + (size_t)r * H * SMLA_NOPE_DIMS,
+                             (uint32_t)(H * SMLA_NOPE_DIMS * 2));
+            bulk_prefetch_l2(static_cast<const uint16_t*>(p.a.q_rope) + (size_t)r * H * SMLA_ROPE_DIMS,
+                             (uint32_t)(H * SMLA_ROPE_DIMS * 2));
+        }
     }
 
     // ---- in-kernel split plan (identical in every CTA; reads live lengths),
@@ -1341,24 +1275,68 @@ __global__ void __launch_bounds__(kThreads, 1) smla_decode_kernel(const KParams 
         dequant_role(c, units, n_units, warp - kDequantWarp0);
     }
 
-    if (*c.abort) err |= SMLA_DEV_TIMEOUT;
     tc_fence_before();
     __syncthreads();
-    // Merges this CTA owes (it arrived last at those rows), with every warp;
-    // the pipeline's shared memory is free now and holds the weights.
-    if (*c.abort == 0u) {
-        uint32_t merge_phase = 0;
-        for (int ui = 0; ui < n_units; ++ui) {
-            if (units[ui].pad0 == 0) continue;
-            __threadfence();
-            merge_row(p, c, units[ui], merge_phase);
-            if (*c.abort) break;
-        }
-    }
+    if (*c.abort) err |= SMLA_DEV_TIMEOUT;
     if (err != 0u) atomicOr(p.err, err);
     if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(c.tmem, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// merge kernel: the partials of split rows -> bf16 out + lse
+// ---------------------------------------------------------------------------
+// One block per (row, dims half, group of kMergeHeads heads), spread over the
+// whole GPU; rows with one partial were finished by the decode kernel and are
+// skipped.  Per head, in split order: M = max(sink, m_i),
+// Z = sum_i l_i 2^(m_i - M) + 2^(sink - M), out = sum_i 2^(m_i - M) O_i / Z,
+// lse = (M + log2 Z) ln 2.  Partials with m = -inf saw no entry and their O is
+// never read; a NaN in a used partial reaches the output.  Thread = (head,
+// 8 dims): the 32 threads of a head read its 1 KB row of each partial.
+constexpr int kMergeHeads = 8;
+constexpr int kMergeThreads = 32 * kMergeHeads;
+
+__global__ void __launch_bounds__(kMergeThreads) smla_merge_kernel(const KParams p) {
+    const smla_decode_args& a = p.a;
+    const int r = blockIdx.x, half = blockIdx.y, H = a.num_heads;
+    const int h = blockIdx.z * kMergeHeads + (int)(threadIdx.x >> 5), q = threadIdx.x & 31;
+    const int2 rt = p.row_table[r];
+    const int u0 = rt.x, sr = rt.y;
+    if (sr <= 1 || h >= H) return;
+    const size_t ml_step = 2 * (size_t)H, po_step = 2 * (size_t)H * 256;  // one unit
+    const float2* ml = p.ml + ((size_t)u0 * 2 + half) * H + h;
+    const float* po = p.po + (((size_t)u0 * 2 + half) * H + h) * 256 + 8 * q;
+    const float sink2 = a.sink != nullptr ? __ldg(a.sink + h) * kLog2e : -INFINITY;
+    float M = sink2;
+    for (int i = 0; i < sr; ++i) M = fmaxf(M, __ldcg(ml + i * ml_step).x);
+    float Z = (M != -INFINITY && sink2 != -INFINITY) ? exp2f(sink2 - M) : 0.f, lall = 0.f;
+    float acc[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+#pragma unroll 4
+    for (int i = 0; i < sr; ++i) {
+        const float2 mi = __ldcg(ml + i * ml_step);
+        const float4 x0 = __ldcg(reinterpret_cast<const float4*>(po + i * po_step));
+        const float4 x1 = __ldcg(reinterpret_cast<const float4*>(po + i * po_step) + 1);
+        lall += mi.y;
+        if (mi.x != -INFINITY) {  // then M is finite
+            const float w = exp2f(mi.x - M);
+            Z += mi.y * w;
+            acc[0] += w * x0.x; acc[1] += w * x0.y; acc[2] += w * x0.z; acc[3] += w * x0.w;
+            acc[4] += w * x1.x; acc[5] += w * x1.y; acc[6] += w * x1.z; acc[7] += w * x1.w;
+        }
+    }
+    const float inv = Z > 0.f ? 1.f / Z : 0.f;
+    uint4 o;
+    o.x = pack_bf16(acc[0] * inv, acc[1] * inv); o.y = pack_bf16(acc[2] * inv, acc[3] * inv);
+    o.z = pack_bf16(acc[4] * inv, acc[5] * inv); o.w = pack_bf16(acc[6] * inv, acc[7] * inv);
+    *reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + ((size_t)r * H + h) * SMLA_HEAD_DIM + 256 * half + 8 * q) = o;
+    if (half == 0 && q == 0 && a.lse != nullptr) {
+        float lse = (M == -INFINITY || Z <= 0.f) ? -INFINITY : (M + log2f(Z)) * kLn2;
+        if (lall == 0.f) lse = a.sink != nullptr ? __ldg(a.sink + h) : -INFINITY;  // sink only, exactly
+        a.lse[(size_t)r * H + h] = lse;
     }
 }
 
@@ -1397,7 +1375,7 @@ smla_status launch_decode(const smla_decode_args* args, void* workspace, cudaStr
     kp.a = *args;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     kp.err = reinterpret_cast<uint32_t*>(ws + L.off_err);
-    kp.counters = reinterpret_cast<uint32_t*>(ws + L.off_counters);
+    kp.row_table = reinterpret_cast<int2*>(ws + L.off_rows);
     kp.ml = reinterpret_cast<float2*>(ws + L.off_ml);
     kp.po = reinterpret_cast<float*>(ws + L.off_po);
     kp.units = args->num_rows * args->num_splits;
@@ -1410,6 +1388,10 @@ smla_status launch_decode(const smla_decode_args* args, void* workspace, cudaStr
     pairs = std::max(pairs, (kp.units + kMaxUnitsPerPair - 1) / kMaxUnitsPerPair);
     const dim3 grid((unsigned)(2 * pairs)), block(kThreads);
     smla_decode_kernel<<<grid, block, kSmemBytes, stream>>>(kp);
+    if (cudaGetLastError() != cudaSuccess) return SMLA_ERR_CUDA;
+    // split rows: a second launch merges their partials across the whole GPU
+    const dim3 mgrid((unsigned)args->num_rows, 2u, (unsigned)((args->num_heads + kMergeHeads - 1) / kMergeHeads));
+    smla_merge_kernel<<<mgrid, kMergeThreads, 0, stream>>>(kp);
     return cudaGetLastError() == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA;
 }
 

@@ -7,12 +7,11 @@
 
 namespace smla {
 
-// Workspace layout.  The error word and the arrival counters sit at fixed
-// offsets so that a workspace stays valid across calls with different row
-// counts: every successful call returns the counters it used to zero.
+// Workspace layout.  The error word and the row table sit at fixed offsets,
+// so that a workspace stays valid across calls with different row counts.
 struct WorkspaceLayout {
     size_t off_err;       // uint32 device error word
-    size_t off_counters;  // uint32 [SMLA_MAX_ROWS][2] arrival counters (row, dim half)
+    size_t off_rows;      // int2 [SMLA_MAX_ROWS] per row: first unit, partials (written by each call)
     size_t off_ml;        // float2 [units][2][H]  per-unit (m, l), one copy per dim half
     size_t off_po;        // float  [units][2][H][256] per-unit unnormalised O by dims half (units = unit_capacity)
     size_t total;
@@ -33,14 +32,14 @@ inline WorkspaceLayout workspace_layout(int rows, int heads, int splits) {
     WorkspaceLayout L;
     const size_t units = (size_t)unit_capacity(rows, splits);
     L.off_err = 0;
-    L.off_counters = 256;
-    L.off_ml = align_up(L.off_counters + sizeof(uint32_t) * 2 * SMLA_MAX_ROWS, 256);
+    L.off_rows = 256;
+    L.off_ml = align_up(L.off_rows + sizeof(int32_t) * 2 * SMLA_MAX_ROWS, 256);
     L.off_po = align_up(L.off_ml + units * 2 * (size_t)heads * 2 * sizeof(float), 256);
     L.total = L.off_po + units * (size_t)heads * SMLA_HEAD_DIM * sizeof(float);
     return L;
 }
 
-// Host-validated launch of the decode kernel (defined in smla_decode.cu).
+// Host-validated launch of the decode and merge kernels (defined in smla_decode.cu).
 smla_status launch_decode(const smla_decode_args* args, void* workspace, cudaStream_t stream);
 
 }  // namespace smla

@@ -55,8 +55,8 @@ extern "C" smla_status smla_decode_static_scratch(const smla_decode_args* args, 
     void* scratch = nullptr;
     const smla_status st = scratch_on_current_device(&scratch);
     if (st != SMLA_OK) return st;
-    // The error word and the arrival counters must start at zero.  The array
-    // keeps whatever the previous call left, so clear them on the stream.
+    // The error word must start at zero.  The array keeps whatever the
+    // previous call left, so clear the head of the layout on the stream.
     const smla::WorkspaceLayout L = smla::workspace_layout(args->num_rows, args->num_heads, args->num_splits);
     if (cudaMemsetAsync(scratch, 0, L.off_ml, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return SMLA_ERR_CUDA;

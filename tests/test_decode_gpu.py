@@ -55,6 +55,16 @@ def test_mixed_split_and_unsplit_rows(cuda_device):
     check(p, num_splits=1, what="mixed s1")
 
 
+def test_one_very_long_row_takes_the_split_budget(cuda_device):
+    # 8 rows at 128 heads with a budget of 8 x 32 units: the chunked plan gives
+    # the long row (64000 compressed entries, ~1000 tiles) as many partials as
+    # the per-row cap allows; its final merge combines them all
+    R = 8
+    p = small(H=128, seq_lens=(2000,) * R, topk=32, swa=16, invalid=0.0, seed=21,
+              cmp_override=([0] * R, [64000] + [16] * (R - 1), 64000))
+    check(p, num_splits=32, what="long row, 32 splits")
+
+
 def test_every_row_one_split_on_wide_grid(cuda_device):
     # grid of rows*splits units where the live lengths give every row one split
     p = small(H=128, seq_lens=(200, 150, 100, 90), topk=32, swa=16, seed=13)
