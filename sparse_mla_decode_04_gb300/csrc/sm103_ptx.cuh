@@ -82,6 +82,16 @@ __device__ __forceinline__ void cp_async_8(uint32_t dst, const void* src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" :: "r"(dst), "l"(src) : "memory");
 }
 
+// Ampere-style async copy of 16 bytes global -> shared, L2 only; src_bytes < 16
+// zero-fills the rest (0: nothing is read).  Waited for by cp_async_wait_all.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" :: "r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 // Arrive on `bar` once all of this thread's earlier cp.async copies have landed
 // (the barrier's expected count includes this arrival).
 __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {

@@ -122,7 +122,7 @@ constexpr uint32_t kSmemBytes = kSmemUsed + 1024;               // + alignment s
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 // The plan's per-row scratch (tiles[R], prefix[R+1]) aliases the raw ring
 // during the prologue, before any producer runs.
-static_assert(4 * (3 * SMLA_MAX_ROWS + 8) <= kNR * kRawStageBytes, "plan scratch fits in the raw ring");
+static_assert(4 * (3 * SMLA_MAX_ROWS + 2 * kMaxStreamRanges + 8) <= kNR * kRawStageBytes, "plan scratch fits in the raw ring");
 
 // mbarrier indices
 enum : uint32_t {
@@ -765,38 +765,32 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, UnitDesc* units, in
                                  (uint32_t)(H * SMLA_ROPE_DIMS * 2));
             }
             // Q in 16-byte chunks j = dims 8j .. 8j + 7 (NoPE chunks 0..55, RoPE
-            // 56..63).  Each warp reads its 32 heads one head per load
-            // instruction (lane = chunk: coalesced), 8 loads in flight.  The
+            // 56..63).  Each warp copies its 32 heads one head per instruction
+            // (lane = chunk: coalesced) with cp.async, all 32 in flight.  The
             // peer dims' 32 chunks go to TMEM (the A operand of QK's first half)
-            // through a row per head staged in the Q region; the own dims' 32
-            // chunks go straight to their place in the Q region, K-major with
+            // through a row per head staged in the Q region; then the own dims'
+            // 32 chunks go straight to their place in the Q region, K-major with
             // the 128-byte swizzle (after every warp has read its staged rows).
+            // Heads beyond num_heads are zero-filled.
             const uint4* qn = static_cast<const uint4*>(a.q_nope) + (size_t)r * H * (SMLA_NOPE_DIMS / 8);
             const uint4* qr = static_cast<const uint4*>(a.q_rope) + (size_t)r * H * (SMLA_ROPE_DIMS / 8);
             const int pbase = 32 * (1 - (int)c.half), obase = 32 * (int)c.half;
 #pragma unroll 1
             for (int pass = 0; pass < 2; ++pass) {
                 const int j = (pass == 0 ? pbase : obase) + lane;
-#pragma unroll 1
-                for (int r0 = 0; r0 < 32; r0 += 8) {
-                    uint4 w[8];
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const int hh = 32 * warp + r0 + k;
-                        w[k] = hh >= H ? make_uint4(0u, 0u, 0u, 0u)
-                                       : (j < 56 ? __ldg(qn + (size_t)hh * (SMLA_NOPE_DIMS / 8) + j)
-                                                 : __ldg(qr + (size_t)hh * (SMLA_ROPE_DIMS / 8) + (j - 56)));
-                    }
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const int hh = 32 * warp + r0 + k;
-                        const uint32_t dst = pass == 0 ? stage_addr(c, hh, lane)
-                                                       : c.sb + kOffQ + (lane >> 3) * 16384 + sw128_offset(hh, lane & 7);
-                        st_shared_v4(dst, w[k].x, w[k].y, w[k].z, w[k].w);
-                    }
+#pragma unroll 8
+                for (int rr = 0; rr < 32; ++rr) {
+                    const int hh = 32 * warp + rr;
+                    const int hs = hh < H ? hh : 0;
+                    const uint4* src = j < 56 ? qn + (size_t)hs * (SMLA_NOPE_DIMS / 8) + j
+                                              : qr + (size_t)hs * (SMLA_ROPE_DIMS / 8) + (j - 56);
+                    const uint32_t dst = pass == 0 ? stage_addr(c, hh, lane)
+                                                   : c.sb + kOffQ + (lane >> 3) * 16384 + sw128_offset(hh, lane & 7);
+                    cp_async_16(dst, src, hh < H ? 16u : 0u);
                 }
+                cp_async_wait_all();
+                __syncwarp();
                 if (pass == 0) {
-                    __syncwarp();
 #pragma unroll 1
                     for (int hc = 0; hc < 4; ++hc) {  // 64 dims -> 32 TMEM columns
                         uint32_t v[32];
@@ -1013,16 +1007,24 @@ __device__ __forceinline__ int row_of_tile(const int* cum, int R, long long pos)
     return lo;
 }
 
-// The stream range q (of Q equal ranges [q T / Q, (q + 1) T / Q)) holding pos,
-// and the start of range q.  32-bit division when T * Q fits (64-bit integer
-// division is a long software sequence).
-__device__ __forceinline__ int stream_range_of(long long pos, long long T, int Q) {
-    if (T * Q < (1LL << 32)) return (int)(((uint32_t)(pos + 1) * (uint32_t)Q - 1u) / (uint32_t)T);
-    return (int)(((pos + 1) * Q - 1) / T);
-}
+// The start of range q of Q equal ranges [q T / Q, (q + 1) T / Q); 32-bit
+// division when T * Q fits (64-bit integer division is a long software
+// sequence).
 __device__ __forceinline__ long long stream_range_start(int q, long long T, int Q) {
     if (T * Q < (1LL << 32)) return (long long)(((uint32_t)q * (uint32_t)T) / (uint32_t)Q);
     return (long long)q * T / Q;
+}
+
+// The range holding tile position pos (0 <= pos < cut[Q]) of strictly
+// increasing cuts cut[0] = 0 < cut[1] < ... < cut[Q]: the last q < Q with
+// cut[q] <= pos.
+__device__ __forceinline__ int cut_range_of(const int* cut, int Q, long long pos) {
+    int lo = 0, hi = Q - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (cut[mid] <= pos) lo = mid; else hi = mid - 1;
+    }
+    return lo;
 }
 
 // out[r] = sum of f(r') for r' < r, r < R, and out[R] = the total; one warp,
@@ -1064,7 +1066,7 @@ __device__ void warp_exclusive_scan(int R, int* out, F f) {
 //      with no tile get one empty unit each, on pair r % Q.
 // Writes this pair's unit list and its length (misc[2]).
 __device__ void plan_warp(const KParams& p, int pair, int n_pairs, UnitDesc* units, volatile uint32_t* misc,
-                          int* s_tiles, int* s_prefix, int* s_cum, uint32_t& plan_err) {
+                          int* s_tiles, int* s_prefix, int* s_cum, int* s_cut, int* s_eacc, uint32_t& plan_err) {
     const smla_decode_args& a = p.a;
     const int lane = threadIdx.x & 31;
     const int R = a.num_rows;
@@ -1102,22 +1104,50 @@ __device__ void plan_warp(const KParams& p, int pair, int n_pairs, UnitDesc* uni
     Q = (int)min((long long)Q, max(1LL, T / kMinStreamTiles));
     bool stream = false;
     if (Q > 1 && T > 0 && Q > min(units_c, n_pairs)) {
-        // upper bound on any pair's unit count: rows met by its range + empty rows
-        int zero_rows = 0, upp = 0;
-        for (int r = lane; r < R; r += 32) zero_rows += s_tiles[r] == 0;
+        // Equal cuts first.  A range that meets e more rows than one pays about
+        // e * kUnitCostTiles more (staging and finishing its extra units), so
+        // the cuts then move to give it that many fewer tiles: cut q sits at
+        // q L - kUnitCostTiles * (e_0 + ... + e_{q-1}), L = (T + kUnitCostTiles E) / Q.
+        // They are kept only if every range stays non-empty.
         for (int q = lane; q < Q; q += 32) {
             const long long ra = stream_range_start(q, T, Q), rb = stream_range_start(q + 1, T, Q);
-            if (ra < rb) upp = max(upp, row_of_tile(s_cum, R, rb - 1) - row_of_tile(s_cum, R, ra) + 1);
+            s_cut[q] = row_of_tile(s_cum, R, rb - 1) - row_of_tile(s_cum, R, ra);  // ra < rb: T >= 4 Q
+        }
+        __syncwarp();
+        warp_exclusive_scan(Q, s_eacc, [&](int q) { return s_cut[q]; });
+        const long long E = s_eacc[Q];
+        for (int q = lane; q <= Q; q += 32)
+            s_cut[q] = q == Q ? (int)T
+                              : (int)(((long long)q * (T + kUnitCostTiles * E) - (long long)kUnitCostTiles * Q * s_eacc[q]) / Q);
+        __syncwarp();
+        bool inc = true;
+        for (int q = lane; q < Q; q += 32) inc = inc && s_cut[q] < s_cut[q + 1];
+        if (!__all_sync(0xffffffffu, inc)) {
+            for (int q = lane; q <= Q; q += 32) s_cut[q] = (int)stream_range_start(q, T, Q);
+        }
+        __syncwarp();
+        // each range's units (rows met, plus its share of empty rows) and the
+        // estimated makespan on the final cuts
+        int zero_rows = 0, upp = 0;
+        long long mk_s = 0;
+        for (int r = lane; r < R; r += 32) zero_rows += s_tiles[r] == 0;
+        for (int q = lane; q < Q; q += 32) {
+            const int ra = s_cut[q], rb = s_cut[q + 1];
+            const int u = row_of_tile(s_cum, R, rb - 1) - row_of_tile(s_cum, R, ra) + 1;
+            upp = max(upp, u);
+            mk_s = max(mk_s, (long long)(rb - ra) + (long long)kUnitCostTiles * u);
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
             zero_rows += __shfl_xor_sync(0xffffffffu, zero_rows, o);
             upp = max(upp, __shfl_xor_sync(0xffffffffu, upp, o));
+            mk_s = max(mk_s, __shfl_xor_sync(0xffffffffu, mk_s, o));
         }
-        upp += min(zero_rows, (R + Q - 1) / Q);  // empty rows r = q, q + Q, ... of one pair
+        const int zero_share = min(zero_rows, (R + Q - 1) / Q);  // empty rows r = q, q + Q, ... of one pair
+        upp += zero_share;
+        mk_s += (long long)kUnitCostTiles * zero_share;
         const long long passes_c = (units_c + n_pairs - 1) / n_pairs;
         const long long mk_c = (long long)chunk * passes_c + kUnitCostTiles * passes_c;
-        const long long mk_s = (T + Q - 1) / Q + (long long)kUnitCostTiles * upp;
         stream = upp <= kMaxUnitsPerPair && mk_s < mk_c;
     }
     if (stream) {
@@ -1125,7 +1155,7 @@ __device__ void plan_warp(const KParams& p, int pair, int n_pairs, UnitDesc* uni
         warp_exclusive_scan(R, s_prefix, [&](int r) {
             const int t = s_tiles[r];
             if (t == 0) return 1;
-            return stream_range_of(s_cum[r + 1] - 1, T, Q) - stream_range_of(s_cum[r], T, Q) + 1;
+            return cut_range_of(s_cut, Q, s_cum[r + 1] - 1) - cut_range_of(s_cut, Q, s_cum[r]) + 1;
         });
     }
     const int total_units = s_prefix[R];
@@ -1135,11 +1165,11 @@ __device__ void plan_warp(const KParams& p, int pair, int n_pairs, UnitDesc* uni
         int n = 0;
         if (stream) {
             if (pair < Q) {
-                const long long ra = stream_range_start(pair, T, Q), rb = stream_range_start(pair + 1, T, Q);
+                const long long ra = s_cut[pair], rb = s_cut[pair + 1];
                 if (ra < rb) {
                     for (int r = row_of_tile(s_cum, R, ra); r < R && s_cum[r] < rb; ++r) {
                         if (s_tiles[r] == 0) continue;
-                        const int q0 = stream_range_of(s_cum[r], T, Q);
+                        const int q0 = cut_range_of(s_cut, Q, s_cum[r]);
                         UnitDesc d;
                         d.row = r;
                         d.row_u0 = s_prefix[r];
@@ -1210,6 +1240,8 @@ __global__ void __launch_bounds__(kThreads, 1) smla_decode_kernel(const KParams 
     int* s_tiles = reinterpret_cast<int*>(smem + kOffRaw);  // prologue only
     int* s_prefix = s_tiles + SMLA_MAX_ROWS;                 // [R + 1]
     int* s_cum = s_prefix + SMLA_MAX_ROWS + 1;               // [R + 1]
+    int* s_cut = s_cum + SMLA_MAX_ROWS + 1;                  // [Q + 1] stream-plan cuts
+    int* s_eacc = s_cut + kMaxStreamRanges + 1;              // [Q + 1]
     UnitDesc* units = reinterpret_cast<UnitDesc*>(smem + kOffUnits);
     const int pair = blockIdx.x >> 1;
     const int n_pairs = gridDim.x >> 1;
@@ -1255,7 +1287,7 @@ __global__ void __launch_bounds__(kThreads, 1) smla_decode_kernel(const KParams 
     // ---- in-kernel split plan (identical in every CTA; reads live lengths),
     //      computed by one warp while the others set up barriers and TMEM ----
     uint32_t plan_err = 0;
-    if (warp == kPlanWarp) plan_warp(p, pair, n_pairs, units, misc, s_tiles, s_prefix, s_cum, plan_err);
+    if (warp == kPlanWarp) plan_warp(p, pair, n_pairs, units, misc, s_tiles, s_prefix, s_cum, s_cut, s_eacc, plan_err);
     if (blockIdx.x == 0 && plan_err) err |= plan_err;
     tc_fence_before();
     __syncthreads();  // barrier inits, TMEM address and unit list visible; plan scratch dead
