@@ -1007,9 +1007,13 @@ __device__ __forceinline__ int row_of_tile(const int* cum, int R, long long pos)
     return lo;
 }
 
-// The start of range q of Q equal ranges [q T / Q, (q + 1) T / Q); 32-bit
-// division when T * Q fits (64-bit integer division is a long software
-// sequence).
+// The equal range q (of Q ranges [q T / Q, (q + 1) T / Q)) holding pos, and
+// the start of range q; 32-bit division when T * Q fits (64-bit integer
+// division is a long software sequence).
+__device__ __forceinline__ int stream_range_of(long long pos, long long T, int Q) {
+    if (T * Q < (1LL << 32)) return (int)(((uint32_t)(pos + 1) * (uint32_t)Q - 1u) / (uint32_t)T);
+    return (int)(((pos + 1) * Q - 1) / T);
+}
 __device__ __forceinline__ long long stream_range_start(int q, long long T, int Q) {
     if (T * Q < (1LL << 32)) return (long long)(((uint32_t)q * (uint32_t)T) / (uint32_t)Q);
     return (long long)q * T / Q;
@@ -1044,8 +1048,9 @@ __device__ void warp_exclusive_scan(int R, int* out, F f) {
     }
     int run = incl - my_sum;
     for (int r = r0; r < r1; ++r) {
+        const int v = f(r);  // read before out[r] is written: f may read out
         out[r] = run;
-        run += f(r);
+        run += v;
     }
     if (lane == 31) out[R] = incl;
     __syncwarp();
@@ -1108,10 +1113,16 @@ __device__ void plan_warp(const KParams& p, int pair, int n_pairs, UnitDesc* uni
         // e * kUnitCostTiles more (staging and finishing its extra units), so
         // the cuts then move to give it that many fewer tiles: cut q sits at
         // q L - kUnitCostTiles * (e_0 + ... + e_{q-1}), L = (T + kUnitCostTiles E) / Q.
-        // They are kept only if every range stays non-empty.
-        for (int q = lane; q < Q; q += 32) {
-            const long long ra = stream_range_start(q, T, Q), rb = stream_range_start(q + 1, T, Q);
-            s_cut[q] = row_of_tile(s_cum, R, rb - 1) - row_of_tile(s_cum, R, ra);  // ra < rb: T >= 4 Q
+        // They are kept only if every range stays non-empty.  e_q counts the
+        // rows (with tiles) that start strictly inside range q: one pass over
+        // the rows, not a search per range.
+        for (int q = lane; q <= Q; q += 32) s_cut[q] = 0;
+        __syncwarp();
+        for (int r = lane + 1; r < R; r += 32) {
+            const long long b0 = s_cum[r];
+            if (s_tiles[r] == 0 || b0 >= T) continue;
+            const int q = stream_range_of(b0, T, Q);
+            if (stream_range_start(q, T, Q) != b0) atomicAdd(&s_cut[q], 1);
         }
         __syncwarp();
         warp_exclusive_scan(Q, s_eacc, [&](int q) { return s_cut[q]; });
@@ -1125,17 +1136,23 @@ __device__ void plan_warp(const KParams& p, int pair, int n_pairs, UnitDesc* uni
         if (!__all_sync(0xffffffffu, inc)) {
             for (int q = lane; q <= Q; q += 32) s_cut[q] = (int)stream_range_start(q, T, Q);
         }
+        // each range's units on the final cuts (the row holding its first tile
+        // plus the rows starting inside it) and the estimated makespan
+        for (int q = lane; q <= Q; q += 32) s_eacc[q] = 1;
         __syncwarp();
-        // each range's units (rows met, plus its share of empty rows) and the
-        // estimated makespan on the final cuts
+        for (int r = lane + 1; r < R; r += 32) {
+            const int b0 = s_cum[r];
+            if (s_tiles[r] == 0 || b0 >= T) continue;
+            const int q = cut_range_of(s_cut, Q, b0);
+            if (s_cut[q] != b0) atomicAdd(&s_eacc[q], 1);
+        }
+        __syncwarp();
         int zero_rows = 0, upp = 0;
         long long mk_s = 0;
         for (int r = lane; r < R; r += 32) zero_rows += s_tiles[r] == 0;
         for (int q = lane; q < Q; q += 32) {
-            const int ra = s_cut[q], rb = s_cut[q + 1];
-            const int u = row_of_tile(s_cum, R, rb - 1) - row_of_tile(s_cum, R, ra) + 1;
-            upp = max(upp, u);
-            mk_s = max(mk_s, (long long)(rb - ra) + (long long)kUnitCostTiles * u);
+            upp = max(upp, s_eacc[q]);
+            mk_s = max(mk_s, (long long)(s_cut[q + 1] - s_cut[q]) + (long long)kUnitCostTiles * s_eacc[q]);
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
@@ -1151,12 +1168,13 @@ __device__ void plan_warp(const KParams& p, int pair, int n_pairs, UnitDesc* uni
         stream = upp <= kMaxUnitsPerPair && mk_s < mk_c;
     }
     if (stream) {
-        // per-row unit counts of the stream plan, then their prefix (unit ids)
-        warp_exclusive_scan(R, s_prefix, [&](int r) {
+        // per-row unit counts of the stream plan, then (in place) their prefix: unit ids
+        for (int r = lane; r < R; r += 32) {
             const int t = s_tiles[r];
-            if (t == 0) return 1;
-            return cut_range_of(s_cut, Q, s_cum[r + 1] - 1) - cut_range_of(s_cut, Q, s_cum[r]) + 1;
-        });
+            s_prefix[r] = t == 0 ? 1 : cut_range_of(s_cut, Q, s_cum[r + 1] - 1) - cut_range_of(s_cut, Q, s_cum[r]) + 1;
+        }
+        __syncwarp();
+        warp_exclusive_scan(R, s_prefix, [&](int r) { return s_prefix[r]; });
     }
     const int total_units = s_prefix[R];
     if (blockIdx.x == 0)  // the merge kernel's map of the partials
