@@ -1340,11 +1340,15 @@ __global__ void __launch_bounds__(kThreads, 1) smla_decode_kernel(const KParams 
 // ---------------------------------------------------------------------------
 // One block per (row, dims half, group of kMergeHeads heads), spread over the
 // whole GPU; rows with one partial were finished by the decode kernel and are
-// skipped.  Per head, in split order: M = max(sink, m_i),
-// Z = sum_i l_i 2^(m_i - M) + 2^(sink - M), out = sum_i 2^(m_i - M) O_i / Z,
-// lse = (M + log2 Z) ln 2.  Partials with m = -inf saw no entry and their O is
-// never read; a NaN in a used partial reaches the output.  Thread = (head,
-// 8 dims): the 32 threads of a head read its 1 KB row of each partial.
+// skipped.  Thread = (head, 8 dims): the 32 threads of a head read its 1 KB
+// row of each partial.  Each thread merges the partials in split order with a
+// running maximum (one pass: every load of a partial is independent of the
+// others): with M = max(sink, m_0..m_i) so far, Z and acc are kept scaled to
+// 2^-M and rescaled when M grows; at the end out = acc / Z and
+// lse = (M + log2 Z) ln 2, equal to the two-pass
+// Z = sum_i l_i 2^(m_i - M) + 2^(sink - M), out = sum_i 2^(m_i - M) O_i / Z.
+// Partials with m = -inf saw no entry and add nothing (their O is not used);
+// a NaN in a used partial reaches the output.
 constexpr int kMergeHeads = 8;
 constexpr int kMergeThreads = 32 * kMergeHeads;
 
@@ -1359,9 +1363,7 @@ __global__ void __launch_bounds__(kMergeThreads) smla_merge_kernel(const KParams
     const float2* ml = p.ml + ((size_t)u0 * 2 + half) * H + h;
     const float* po = p.po + (((size_t)u0 * 2 + half) * H + h) * 256 + 8 * q;
     const float sink2 = a.sink != nullptr ? __ldg(a.sink + h) * kLog2e : -INFINITY;
-    float M = sink2;
-    for (int i = 0; i < sr; ++i) M = fmaxf(M, __ldcg(ml + i * ml_step).x);
-    float Z = (M != -INFINITY && sink2 != -INFINITY) ? exp2f(sink2 - M) : 0.f, lall = 0.f;
+    float M = sink2, Z = sink2 != -INFINITY ? 1.f : 0.f, lall = 0.f;
     float acc[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[j] = 0.f;
@@ -1371,12 +1373,18 @@ __global__ void __launch_bounds__(kMergeThreads) smla_merge_kernel(const KParams
         const float4 x0 = __ldcg(reinterpret_cast<const float4*>(po + i * po_step));
         const float4 x1 = __ldcg(reinterpret_cast<const float4*>(po + i * po_step) + 1);
         lall += mi.y;
-        if (mi.x != -INFINITY) {  // then M is finite
-            const float w = exp2f(mi.x - M);
-            Z += mi.y * w;
-            acc[0] += w * x0.x; acc[1] += w * x0.y; acc[2] += w * x0.z; acc[3] += w * x0.w;
-            acc[4] += w * x1.x; acc[5] += w * x1.y; acc[6] += w * x1.z; acc[7] += w * x1.w;
+        if (mi.x == -INFINITY) continue;
+        if (mi.x > M) {  // the running maximum grows: rescale what is summed so far
+            const float f = M == -INFINITY ? 0.f : exp2f(M - mi.x);
+            Z *= f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[j] *= f;
+            M = mi.x;
         }
+        const float w = exp2f(mi.x - M);
+        Z += mi.y * w;
+        acc[0] += w * x0.x; acc[1] += w * x0.y; acc[2] += w * x0.z; acc[3] += w * x0.w;
+        acc[4] += w * x1.x; acc[5] += w * x1.y; acc[6] += w * x1.z; acc[7] += w * x1.w;
     }
     const float inv = Z > 0.f ? 1.f / Z : 0.f;
     uint4 o;
