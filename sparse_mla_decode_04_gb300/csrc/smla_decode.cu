@@ -134,8 +134,8 @@ enum : uint32_t {
     BAR_XP_EMPTY = BAR_XO_EMPTY + kNXO,    // MMA commit after QK (peer dims free)
     BAR_S_FULL = BAR_XP_EMPTY + 1,         // [2] MMA commit after QK
     BAR_P_FULL = BAR_S_FULL + 2,           // [2] softmax -> MMA (kSoftmaxWarps)
-    BAR_O_DONE = BAR_P_FULL + 2,           // MMA commit after each PV
-    BAR_Q_READY = BAR_O_DONE + 1,          // softmax -> MMA, once per unit (kSoftmaxWarps)
+    BAR_O_DONE = BAR_P_FULL + 2,           // [2] MMA commit after PV(j), on barrier j % 2
+    BAR_Q_READY = BAR_O_DONE + 2,          // softmax -> MMA, once per unit (kSoftmaxWarps)
     BAR_MMA_FINAL = BAR_Q_READY + 1,       // teardown: all MMAs retired
     BAR_COUNT = BAR_MMA_FINAL + 1
 };
@@ -640,7 +640,7 @@ __device__ __forceinline__ bool issue_pv(const Ctx& c, uint32_t j, bool first_of
             mma_bf16_ts(c.tmem + kTmemO, tp + 16 * kk + 8, bd0 + (uint64_t)(kk * 2048 >> 4), idesc_pv, 1u);
     }
     mma_commit(bar_addr(c, BAR_XO_EMPTY + xs));
-    mma_commit(bar_addr(c, BAR_O_DONE));
+    mma_commit(bar_addr(c, BAR_O_DONE + (j & 1u)));
     return true;
 }
 
@@ -673,7 +673,7 @@ __device__ void mma_role(const Ctx& c, const UnitDesc* units, int n_units) {
 #pragma unroll 1
             for (int part = 0; part < 2; ++part) {
                 if (part == 0) {
-#pragma unroll 4
+#pragma unroll
                     for (int kk = 0; kk < 16; ++kk)
                         mma_bf16_ts(ts, c.tmem + kTmemQ + kk * 8,
                                     xp_desc0 + (uint64_t)(((kk >> 2) * kAtomBytes + (kk & 3) * 32) >> 4), idesc_qk,
@@ -681,7 +681,7 @@ __device__ void mma_role(const Ctx& c, const UnitDesc* units, int n_units) {
                 } else {
                     if (!wait_bar(c, bar_addr(c, BAR_X_FULL + xs), (g / kNXO) & 1u)) { ok = false; break; }
                     tc_fence_after();
-#pragma unroll 4
+#pragma unroll
                     for (int kk = 0; kk < 16; ++kk)
                         mma_bf16_ss(ts, q_desc0 + (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4),
                                     xo_desc0 + (uint64_t)(((kk >> 2) * kAtomBytes + (kk & 3) * 32) >> 4), idesc_qk, 1u);
@@ -745,7 +745,7 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, UnitDesc* units, in
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     const float qscale = a.sm_scale * kLog2e;
     const float sink2 = (a.sink != nullptr && h < H) ? __ldg(a.sink + h) * kLog2e : -INFINITY;
-    uint32_t g = 0, pv = 0;
+    uint32_t g = 0;
     bool ok = true;
 
     for (int ui = 0; ui < n_units && ok; ++ui) {
@@ -885,14 +885,17 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, UnitDesc* units, in
             }
             lsum = lsum * alpha + ps;
             skipped *= alpha;
-            // PV(g-1) must be done before O is rescaled (its completion is consumed
-            // once per tile to keep the barrier's phases in step).
-            if (i > 0) {
-                if (!wait_bar_warp(c, bar_addr(c, BAR_O_DONE), pv & 1u)) { ok = false; break; }
-                ++pv;
+            // PV(g-1) must be done before O is rescaled; without a rescale this
+            // warp does not wait for it.  Every tile has one PV, PV(j) commits to
+            // O_DONE[j % 2], and S_FULL(g) (QK(g) retired, issued after PV(g-2))
+            // means PV(g-3) has retired: the barrier is at most one phase behind
+            // the one waited for, so a parity wait cannot alias.
+            const bool need_o = __any_sync(0xffffffffu, rescale);
+            if (need_o) {
+                if (!wait_bar_warp(c, bar_addr(c, BAR_O_DONE + ((g - 1) & 1u)), ((g - 1) >> 1) & 1u)) { ok = false; break; }
                 tc_fence_after();
             }
-            if (__any_sync(0xffffffffu, rescale)) {
+            if (need_o) {
                 const float f = rescale ? alpha : 1.f;
 #pragma unroll 1
                 for (int cc = 0; cc < 8; ++cc) {
@@ -922,9 +925,8 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, UnitDesc* units, in
             if (lane == 0) mbar_arrive_local(bar_addr(c, BAR_P_FULL + sbuf));
             o_init = true;
         }
-        if (ok && n > 0) {
-            if (!wait_bar_warp(c, bar_addr(c, BAR_O_DONE), pv & 1u)) ok = false;
-            ++pv;
+        if (ok && n > 0) {  // the unit's last PV (PV(g-1)); earlier ones retired before it
+            if (!wait_bar_warp(c, bar_addr(c, BAR_O_DONE + ((g - 1) & 1u)), ((g - 1) >> 1) & 1u)) ok = false;
             tc_fence_after();
         }
         if (!softmax_all(ok)) {  // uniform over the softmax warps from here on
@@ -1282,6 +1284,7 @@ __global__ void __launch_bounds__(kThreads, 1) smla_decode_kernel(const KParams 
             mbar_init(bar_addr(c, BAR_P_FULL + i), kSoftmaxWarps);
         }
         mbar_init(bar_addr(c, BAR_O_DONE), 1);
+        mbar_init(bar_addr(c, BAR_O_DONE + 1), 1);
         mbar_init(bar_addr(c, BAR_Q_READY), kSoftmaxWarps);
         mbar_init(bar_addr(c, BAR_MMA_FINAL), 1);
         fence_mbar_init_cluster();
