@@ -848,6 +848,18 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, UnitDesc* units, in
             const float msub = (m_new == -INFINITY) ? 0.f : m_new;
             const bool rescale = o_init && (m_new != m_used);
             m_used = m_new;
+            // A cold tile: for every head of this warp, dropping the tile's whole
+            // lo half keeps the skipped total within the budget on the bound
+            // alone (p <= 2^(mt - m) per entry, |lo| <= p 2^-9 by bf16 rounding,
+            // and the new denominator is at least lsum alpha).  Then lo is not
+            // computed: it is stored as 0 and that bound stands in for its sum.
+            const uint32_t vb = c.sb + kOffXVmax + xs * (4 * kNumDequantWarps);
+            float vmax = ld_shared_f32(vb);
+#pragma unroll
+            for (int w = 1; w < kNumDequantWarps; ++w) vmax = fmaxf(vmax, ld_shared_f32(vb + 4 * w));
+            const float lo_cap = (mt == -INFINITY) ? 0.f
+                                                   : 64.f * ex2_approx(mt - msub) * (1.0f / 512.0f) * (1.0f + 1.0f / 256.0f);
+            const bool cold = __all_sync(0xffffffffu, (h >= H) || (skipped * alpha + lo_cap * vmax <= kLoBudget * lsum * alpha));
             // ---- pass 2: P = 2^(s - m) as a bf16 pair hi = bf16(p), lo = bf16(p - hi),
             // written back over the scores one 16-entry step at a time: entries
             // 16 q .. 16 q + 15 (columns [16 q, 16 q + 16)) become hi in columns
@@ -871,17 +883,21 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, UnitDesc* units, in
                         const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
                         sm[j & 3] += p0 + p1;
                         const __nv_bfloat162 hb = __floats2bfloat162_rn(p0, p1);
-                        const float r0 = p0 - __low2float(hb), r1 = p1 - __high2float(hb);
                         memcpy(&hv[j], &hb, 4);
-                        lv[j] = pack_bf16(r0, r1);
-                        la[j & 3] += fabsf(r0) + fabsf(r1);
+                        if (cold) {
+                            lv[j] = 0u;
+                        } else {
+                            const float r0 = p0 - __low2float(hb), r1 = p1 - __high2float(hb);
+                            lv[j] = pack_bf16(r0, r1);
+                            la[j & 3] += fabsf(r0) + fabsf(r1);
+                        }
                     }
                     tmem_st8(ts + 16 * q, hv);
                     tmem_st8(ts + 16 * q + 8, lv);
                 }
                 ps = (sm[0] + sm[1]) + (sm[2] + sm[3]);
                 // |bf16(r)| <= |r| (1 + 2^-8): a bound on the sum of |lo|
-                lo_abs = ((la[0] + la[1]) + (la[2] + la[3])) * (1.0f + 1.0f / 256.0f);
+                lo_abs = cold ? lo_cap : ((la[0] + la[1]) + (la[2] + la[3])) * (1.0f + 1.0f / 256.0f);
             }
             lsum = lsum * alpha + ps;
             skipped *= alpha;
@@ -909,12 +925,8 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, UnitDesc* units, in
             }
             // vote on skipping the lo half: sum|lo| x max|V| (this CTA's dims) bounds what skipping drops
             {
-                const uint32_t vb = c.sb + kOffXVmax + xs * (4 * kNumDequantWarps);
-                float vmax = ld_shared_f32(vb);
-#pragma unroll
-                for (int w = 1; w < kNumDequantWarps; ++w) vmax = fmaxf(vmax, ld_shared_f32(vb + 4 * w));
                 const float cand = skipped + lo_abs * vmax;
-                const bool mine = (h >= H) || (cand <= kLoBudget * lsum);
+                const bool mine = (h >= H) || cold || (cand <= kLoBudget * lsum);
                 const bool warp_ok = __all_sync(0xffffffffu, mine);
                 if (warp_ok) skipped = cand;  // counted even if another warp vetoes: conservative
                 if (lane == 0) st_shared_u32(c.sb + kOffVote + (sbuf * 4 + warp) * 4, warp_ok ? 1u : 0u);
