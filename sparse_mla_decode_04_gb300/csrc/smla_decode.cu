@@ -437,8 +437,10 @@ __device__ void producer_role(const KParams& p, const Ctx& c, const UnitDesc* un
             }
             const uint32_t mask = __ballot_sync(0xffffffffu, ep != nullptr);
             // A run of consecutive pool rows in lanes 0..n-1 (compressed entries,
-            // window entries within a page) moves as one bulk copy; other tiles
-            // take one copy per entry.
+            // window entries within a page) moves as one bulk copy.  Other tiles
+            // are gathered with 16-byte cp.async (4 lanes per entry, 8 entries
+            // per instruction): 36 instructions per lane instead of 32 bulk
+            // copies queued on the TMA unit.
             const uint8_t* ep0 = reinterpret_cast<const uint8_t*>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(ep), 0));
             const int nvalid = __popc(mask);
             const bool run = (mask == (nvalid == 32 ? 0xffffffffu : (1u << nvalid) - 1u)) &&
@@ -452,13 +454,27 @@ __device__ void producer_role(const KParams& p, const Ctx& c, const UnitDesc* un
             }
             if (!wait_bar_warp(c, bar_addr(c, BAR_RAW_EMPTY + rs), rph ^ 1u)) return;
             const uint32_t full = bar_addr(c, BAR_RAW_FULL + rs);
-            if (lane == 0) mbar_expect_tx_only(full, (uint32_t)nvalid * SMLA_ENTRY_BYTES);
-            __syncwarp();
             const uint32_t dst = c.sb + kOffRaw + rs * kRawStageBytes;
             if (run) {
-                if (lane == 0 && nvalid > 0) bulk_g2s(dst, ep0, (uint32_t)nvalid * SMLA_ENTRY_BYTES, full);
-            } else if (ep != nullptr) {
-                bulk_g2s(dst + lane * SMLA_ENTRY_BYTES, ep, SMLA_ENTRY_BYTES, full);
+                if (lane == 0 && nvalid > 0) {
+                    mbar_expect_tx_only(full, (uint32_t)nvalid * SMLA_ENTRY_BYTES);
+                    bulk_g2s(dst, ep0, (uint32_t)nvalid * SMLA_ENTRY_BYTES, full);
+                }
+            } else {
+#pragma unroll 1
+                for (int rnd = 0; rnd < kRawBK / 8; ++rnd) {
+                    const int e = 8 * rnd + (lane >> 2);
+                    const uint8_t* src = reinterpret_cast<const uint8_t*>(
+                        __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(ep), e));
+                    if (src != nullptr) {
+                        const uint32_t d = dst + (uint32_t)e * SMLA_ENTRY_BYTES;
+#pragma unroll
+                        for (int j = 0; j < SMLA_ENTRY_BYTES / 64; ++j) {
+                            const int k = (lane & 3) + 4 * j;  // 16-byte chunk of the entry
+                            cp_async_16(d + 16 * k, src + 16 * k, 16u);
+                        }
+                    }
+                }
             }
             if (ep != nullptr) cp_async_8(c.sb + kOffRawSc + (rs * kRawBK + lane) * 8, sp);
             cp_async_arrive_noinc(full);  // one of the 32 async arrivals
