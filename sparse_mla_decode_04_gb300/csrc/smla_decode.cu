@@ -1115,30 +1115,14 @@ __device__ void plan_warp(const KParams& p, int pair, int n_pairs, UnitDesc* uni
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) max_t = max(max_t, __shfl_xor_sync(0xffffffffu, max_t, o));
     __syncwarp();
-    int lo = 1, hi = max_t;
-    while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        long long cnt = 0;
-        for (int r = lane; r < R; r += 32) cnt += max(1, ceil_div_i(s_tiles[r], mid));
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
-        if (cnt <= budget) hi = mid; else lo = mid + 1;
-    }
-    const int chunk = lo;
     warp_exclusive_scan(R, s_cum, [&](int r) { return s_tiles[r]; });
-    warp_exclusive_scan(R, s_prefix, [&](int r) {
-        const int t = s_tiles[r];
-        int sr = max(1, ceil_div_i(t, chunk));
-        if (t > 0) sr = ceil_div_i(t, ceil_div_i(t, sr));
-        return sr;
-    });
     const long long T = s_cum[R];
-    const int units_c = s_prefix[R];
-    // candidate (b): Q ranges, each at least kMinStreamTiles tiles long
+    // candidate (b), first: Q ranges, each at least kMinStreamTiles tiles long
     int Q = min(min(n_pairs, p.unit_cap - R + 1), kMaxStreamRanges);
     Q = (int)min((long long)Q, max(1LL, T / kMinStreamTiles));
-    bool stream = false;
-    if (Q > 1 && T > 0 && Q > min(units_c, n_pairs)) {
+    bool stream_ok = false;
+    long long mk_s = 0;
+    if (Q > 1 && T > 0) {
         // Equal cuts first.  A range that meets e more rows than one pays about
         // e * kUnitCostTiles more (staging and finishing its extra units), so
         // the cuts then move to give it that many fewer tiles: cut q sits at
@@ -1178,7 +1162,6 @@ __device__ void plan_warp(const KParams& p, int pair, int n_pairs, UnitDesc* uni
         }
         __syncwarp();
         int zero_rows = 0, upp = 0;
-        long long mk_s = 0;
         for (int r = lane; r < R; r += 32) zero_rows += s_tiles[r] == 0;
         for (int q = lane; q < Q; q += 32) {
             upp = max(upp, s_eacc[q]);
@@ -1193,9 +1176,35 @@ __device__ void plan_warp(const KParams& p, int pair, int n_pairs, UnitDesc* uni
         const int zero_share = min(zero_rows, (R + Q - 1) / Q);  // empty rows r = q, q + Q, ... of one pair
         upp += zero_share;
         mk_s += (long long)kUnitCostTiles * zero_share;
+        stream_ok = upp <= kMaxUnitsPerPair;
+    }
+    // Candidate (a) only when it can win.  With a budget of at most one pass
+    // over the pairs its makespan is chunk + kUnitCostTiles, and the chunk is at
+    // least T / budget (the budget's units must cover every tile); a stream
+    // makespan below that bound wins without computing the chunks.
+    bool stream = stream_ok && p.units <= n_pairs &&
+                  mk_s < (T + budget - 1) / budget + (long long)kUnitCostTiles;
+    if (!stream) {
+        int lo = 1, hi = max_t;
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            long long cnt = 0;
+            for (int r = lane; r < R; r += 32) cnt += max(1, ceil_div_i(s_tiles[r], mid));
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+            if (cnt <= budget) hi = mid; else lo = mid + 1;
+        }
+        const int chunk = lo;
+        warp_exclusive_scan(R, s_prefix, [&](int r) {
+            const int t = s_tiles[r];
+            int sr = max(1, ceil_div_i(t, chunk));
+            if (t > 0) sr = ceil_div_i(t, ceil_div_i(t, sr));
+            return sr;
+        });
+        const int units_c = s_prefix[R];
         const long long passes_c = (units_c + n_pairs - 1) / n_pairs;
         const long long mk_c = (long long)chunk * passes_c + kUnitCostTiles * passes_c;
-        stream = upp <= kMaxUnitsPerPair && mk_s < mk_c;
+        stream = stream_ok && Q > min(units_c, n_pairs) && mk_s < mk_c;
     }
     if (stream) {
         // per-row unit counts of the stream plan, then (in place) their prefix: unit ids
