@@ -22,9 +22,11 @@
 // cost per entry); entries are fetched in 32-entry raw tiles, two per tile.
 //
 //   producer warps (3)   one per raw stage: resolve a raw tile's 32 slots (top-k index -> page
-//                        table -> 64-bit row; window; compressed) and issue one
-//                        bulk copy per valid entry (576 B) plus a cp.async of
-//                        its 8 scale bytes into a 3-stage raw ring;
+//                        table -> 64-bit row; window; compressed) and fetch the
+//                        valid entries (576 B each) into a 3-stage raw ring: one
+//                        bulk copy for a run of consecutive pool rows, else
+//                        16-byte cp.async gathers; plus a cp.async of each
+//                        entry's 8 scale bytes;
 //   dequant warps (8)    raw ring -> bf16 (e4m3 x 2^(code-127), exact) in
 //                        128-byte-swizzled [4 atoms][64][128 B] halves of a
 //                        tile: this CTA's 256 dims ("own": the K-major B of QK
@@ -34,6 +36,7 @@
 //   MMA warp (1 thread)  QK(t): M = 128 heads, N = 64, K = 512 with Q's peer
 //                        dims from TMEM and its own dims from shared memory;
 //                        then PV(t-1): M = 128, N = 256, K = 64 with P from TMEM;
+//                        the issue rate of this one thread bounds the tile;
 //   softmax warps (4)    one thread per head (TMEM lane): online softmax with a
 //                        conditional rescale, P written back over the scores as
 //                        a bf16 pair hi = bf16(p), lo = bf16(p - hi).  A single
@@ -46,8 +49,10 @@
 //
 // TMEM (512 columns): O [0, 256), two score/P buffers [256, 320) and
 // [320, 384), Q's peer dims (the 256 this CTA does not output) as bf16 pairs
-// [384, 512).  Heads beyond num_heads
-// are zero-padded up to the MMA's M = 128.
+// [384, 512).  Heads beyond num_heads are zero-padded up to the MMA's M = 128.
+//
+// Split rows leave fp32 partials; a second launch (smla_merge_kernel, one
+// block per row, dim half and 8 heads) combines them over the whole GPU.
 #include <algorithm>
 #include <cstdint>
 #include <cstring>
