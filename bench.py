@@ -1,13 +1,20 @@
 #!/usr/bin/env python3
 """Benchmark: sparse-MLA decode on GB300, one JSON line on stdout.
 
-A step is one decode call over one batch: the DeepSeek-V4-like decode
-workload (32 rows x 128 heads, 32K context in 64-token pages, top-k 2048
-with 2% invalid slots, window 128, 8192 compressed entries per row) by
-default.  Inputs are resident in HBM; L2 is flushed (a 512 MB write) before
-every timed step; each step replays a CUDA graph holding the call's two
-launches (the decode kernel, then the merge kernel for split rows) and is
-timed with CUDA events on that stream.
+A step is one decode call over one batch.  The default workload is the
+largest single-GPU shape of the T x context matrix: 64 rows x 128 heads at a
+1M-token context (64-token pages, top-k 2048 with 5% invalid slots, window
+128, 262144 compressed entries per row; 16.9M attended entries per call).
+Inputs are resident in HBM; L2 is flushed (a 512 MB write) before every
+timed step; each step replays a CUDA graph holding the call's two launches
+(the decode kernel, then the merge kernel for split rows) and is timed with
+CUDA events on that stream.
+
+The same JSON line carries ``per_config``: the same measurement on the
+DeepSeek-V4-like decode (32 x 32K), the MTP decode (16 x 4 tokens, H = 64),
+the long-context ragged call (contexts 4K/100K/500K/1M, one graph capture
+replayed with re-drawn lengths) and the long-context sweep shapes
+(T in {16, 64} x context in {100K, 500K, 1M}).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
@@ -35,6 +42,9 @@ sys.path.insert(0, ROOT)
 
 METRIC = "sparse-MLA decode µs/call & query-rows/s; % of HBM/tensor roofline, 1×GB300"
 KERNEL_NAME = "smla_decode_kernel"
+DEFAULT_WORKLOAD = "sweep_T64_ctx1048576"
+PER_CONFIG = ("dsv4", "mtp", "ragged", "sweep_T16_ctx102400", "sweep_T16_ctx512000", "sweep_T16_ctx1048576",
+              "sweep_T64_ctx102400", "sweep_T64_ctx512000")
 LAUNCHES_PER_CALL = 2  # smla_decode enqueues the decode kernel and the merge kernel
 KERNEL_SRC = os.path.join(ROOT, "sparse_mla_decode_04_gb300", "csrc", "smla_decode.cu")
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -258,6 +268,8 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "query-rows/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec_per_row * p.num_rows * 1e3,
         "us_per_call": sec_per_row * p.num_rows * 1e6,
+        "ms_per_step_kind": (f"extrapolated: mean oracle time per row x {p.num_rows} rows; each step ran "
+                             f"{sample_rows} row(s) of the call, not the whole call"),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": workload_config(p, S, args.workload),
         "cpu_baseline": {"value": value, "unit": "query-rows/s", "cores": cores, "kind": "oracle",
@@ -270,7 +282,92 @@ def run_reference(args):
 
 
 # ---------------------------------------------------------------------------
+def roofline(flops: float, nbytes: float, t_s: float, peaks: dict) -> dict:
+    """The slower of the algorithmic bytes at HBM bandwidth and the algorithmic
+    flops at the bf16 tensor peak sets the bound; achieved is the work of that
+    bound divided by the measured time."""
+    t_tc = flops / (peaks["bf16_tflops"] * 1e12)
+    t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
+    if t_tc >= t_hbm:
+        achieved, peak, unit, bound = flops / t_s / 1e12, peaks["bf16_tflops"], "TFLOP/s", "tensor"
+    else:
+        achieved, peak, unit, bound = nbytes / t_s / 1e9, peaks["hbm_gbs"], "GB/s", "hbm"
+    return {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+            "t_roofline_us": max(t_tc, t_hbm) * 1e6}
+
+
+def time_call(p, S, ws, steps: int, warmup: int, flush_buf, stream, redraw: bool = False):
+    """Capture one smla_decode call in a CUDA graph and time `steps` replays
+    with CUDA events on the launching stream, L2 flushed before each.  With
+    `redraw`, every replay (warm-up included) first draws new live lengths for
+    all rows (the graph was captured once, at the construction-time lengths).
+    Returns (per-step ms, per-step algorithmic flops, per-step bytes)."""
+    import torch
+    import smla_inputs as I
+    import sparse_mla_decode_04_gb300 as smla
+
+    dev = p.q_nope.device
+    R, H = p.num_rows, p.num_heads
+    out = torch.empty((R, H, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((R, H), dtype=torch.float32, device=dev)
+    with torch.cuda.stream(stream):
+        smla.decode(p, num_splits=S, out=out, lse=lse, workspace=ws)  # attrs + first launch outside capture
+        stream.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            smla.decode(p, num_splits=S, out=out, lse=lse, workspace=ws)
+    ms, flops, nbytes = [], [], []
+    for i in range(warmup + steps):
+        if redraw:
+            I.redraw_lengths(p, seed=7000 + i)
+            torch.cuda.synchronize()
+        f, b = p.algorithmic_flops(), p.algorithmic_bytes()
+        with torch.cuda.stream(stream):
+            flush_buf.fill_(i & 0xFF)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            graph.replay()
+            e1.record(stream)
+        stream.synchronize()
+        if i >= warmup:
+            ms.append(e0.elapsed_time(e1))
+            flops.append(f)
+            nbytes.append(b)
+    del graph
+    return ms, flops, nbytes
+
+
+def per_config_lines(names, dev, flush_buf, stream, peaks, steps: int, warmup: int):
+    """One entry per named workload: µs per call, rows/s and the roofline."""
+    import gc
+    import torch
+    import sparse_mla_decode_04_gb300 as smla
+
+    res = {}
+    for name in names:
+        p = make_workload(name, dev)
+        R, H = p.num_rows, p.num_heads
+        S = smla.smla_plan_num_splits(R, H, p.kv_len_estimate())
+        ws = smla.Workspace(R, H, S, device=dev)
+        ms, fl, nb = time_call(p, S, ws, steps, warmup, flush_buf, stream, redraw=(name == "ragged"))
+        t = statistics.mean(ms) / 1e3
+        rf = roofline(statistics.mean(fl), statistics.mean(nb), t, peaks)
+        flags = ws.read_error()
+        res[name] = {"workload": p.name, "us_per_call": t * 1e6, "rows_per_s": R / t, "rows": R, "heads": H,
+                     "num_splits": S, "valid_entries": int(round(statistics.mean(fl) / (H * 2048))),
+                     "roofline": rf, "device_error": flags,
+                     "timing": ("one graph capture, replayed with re-drawn lengths before each step"
+                                if name == "ragged" else "graph replay, L2 flushed") + f"; {steps} steps"}
+        log(f"per_config {name}: {t * 1e6:.1f} us/call, frac {rf['frac']:.3f}")
+        del p, ws
+        gc.collect()
+        torch.cuda.empty_cache()
+    return res
+
+
 def run_gpu(args):
+    import gc
     import torch
     import torch.distributed as dist
 
@@ -285,7 +382,6 @@ def run_gpu(args):
     smla.build()
     p = make_workload(args.workload, dev)
     if rank > 0:  # replicas draw different data
-        import smla_inputs as I  # noqa: F401
         p.q_nope.copy_(torch.randn_like(p.q_nope, dtype=torch.float32).to(torch.bfloat16))
     R, H = p.num_rows, p.num_heads
     S = args.splits or smla.smla_plan_num_splits(R, H, p.kv_len_estimate())
@@ -335,6 +431,7 @@ def run_gpu(args):
     flags = ws.read_error()
     if flags:
         raise SystemExit(f"device error word set during the bench: {flags:#x}")
+    del graph
 
     # ---- end to end through the public API with host buffers ----
     host_in = {k: getattr(p, k).cpu().pin_memory() for k in
@@ -366,13 +463,7 @@ def run_gpu(args):
     flops = p.algorithmic_flops()
     nbytes = p.algorithmic_bytes()
     t_s = ms_step / 1e3
-    t_tc = flops / (peaks["bf16_tflops"] * 1e12)
-    t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
-    bound = "tensor" if t_tc >= t_hbm else "hbm"
-    if bound == "tensor":
-        achieved, peak, unit = flops / t_s / 1e12, peaks["bf16_tflops"], "TFLOP/s"
-    else:
-        achieved, peak, unit = nbytes / t_s / 1e9, peaks["hbm_gbs"], "GB/s"
+    rf = roofline(flops, nbytes, t_s, peaks)
     traffic = profiled_traffic(args.workload)
     rows_total = R * world
     line = {
@@ -381,12 +472,10 @@ def run_gpu(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded; FP8-e4m3 N(0,1) payload, UE8M0 codes 120..134, bf16 RoPE/q)",
         "config": workload_config(p, S, args.workload) | {"parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
-        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
-                     "traffic": traffic, "peak_source": f"{peak_src} (MEASURED_PEAKS.json burst)"
-                     if peak_src == "measured" else "fallback",
-                     "algorithmic_bytes": nbytes, "algorithmic_flops": flops,
-                     "t_roofline_us": max(t_tc, t_hbm) * 1e6,
-                     "kernel": f"{KERNEL_NAME} (timed with smla_merge_kernel: the whole call)"},
+        "roofline": rf | {"traffic": traffic, "peak_source": f"{peak_src} (MEASURED_PEAKS.json burst)"
+                          if peak_src == "measured" else "fallback",
+                          "algorithmic_bytes": nbytes, "algorithmic_flops": flops,
+                          "kernel": f"{KERNEL_NAME} (timed with smla_merge_kernel: the whole call)"},
         "e2e": {"value": rows_total / (e2e_step / 1e3), "unit": "query-rows/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_step},
         "gpu_launches": LAUNCHES_PER_CALL * args.steps,
@@ -398,6 +487,12 @@ def run_gpu(args):
         line["cpu_baseline"] = {"value": 1.0 / per_row, "unit": "query-rows/s", "cores": cores, "kind": "oracle",
                                 "sample": f"{n_rows} of {R} rows of the same workload, float64 NumPy oracle "
                                           f"(~{args.cpu_budget:.0f} s budget)"}
+    del p, ws, out, lse, host_in
+    gc.collect()
+    torch.cuda.empty_cache()
+    if rank == 0 and world == 1 and not args.no_per_config:
+        names = [n for n in PER_CONFIG if n != args.workload]
+        line["per_config"] = per_config_lines(names, dev, flush_buf, stream, peaks, args.config_steps, 3)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -411,10 +506,12 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="dsv4")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--splits", type=int, default=0, help="override the planner's split count")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true", help="time only the main workload")
+    ap.add_argument("--config-steps", type=int, default=10, help="timed steps per per_config workload")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")

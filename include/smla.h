@@ -189,8 +189,13 @@ smla_status smla_read_device_error(void* workspace, uint32_t* flags, smla_stream
 /* Static, NUL-terminated description of a status code. */
 const char* smla_status_string(smla_status status);
 
-/* Bytes of the scratch array built into the library for smla_decode_static_scratch. */
-#define SMLA_STATIC_SCRATCH_BYTES (32u * 1024u * 1024u)
+/* Bytes of the scratch array built into the library for smla_decode_static_scratch
+ * (48 MiB).  It holds the workspace layout of smla_workspace_bytes: with
+ * U = max(num_rows * num_splits, num_rows + 95) partial units of
+ * num_heads * 2064 bytes each, plus 8.5 KB.  At 128 heads that is U <= 190:
+ * num_rows <= 95 and num_rows * num_splits <= 190 (the 32-row x 128-head
+ * DeepSeek-V4-like decode fits at up to 5 splits). */
+#define SMLA_STATIC_SCRATCH_BYTES (48u * 1024u * 1024u)
 
 /*
  * smla_decode for callers that cannot allocate device memory.  The pages have
@@ -202,13 +207,16 @@ const char* smla_status_string(smla_status status);
  * processes whose device memory is owned entirely by another allocator.  This
  * entry point allocates nothing: its scratch (the same layout as the
  * smla_decode workspace) is a file-scope __device__ array of
- * SMLA_STATIC_SCRATCH_BYTES (32 MiB) that every GPU which loads the library
+ * SMLA_STATIC_SCRATCH_BYTES (48 MiB) that every GPU which loads the library
  * holds until the process exits.  The caller still passes every input and
  * output in `args`.
  *
  * - Calls whose smla_workspace_bytes(num_rows, num_heads, num_splits) exceeds
  *   SMLA_STATIC_SCRATCH_BYTES return SMLA_ERR_WORKSPACE_TOO_SMALL and launch
- *   nothing; shrink num_splits or the batch.
+ *   nothing.  The workspace always holds at least num_rows + 95 units, so
+ *   lowering num_splits helps only while num_rows * num_splits is the larger
+ *   term; beyond the limit given with SMLA_STATIC_SCRATCH_BYTES, split the
+ *   batch into several calls.
  * - The first call on a device looks up the array's device address
  *   (cudaGetSymbolAddress, with that device current) and caches it; make that
  *   first call before any stream capture on the device.
@@ -217,7 +225,9 @@ const char* smla_status_string(smla_status status);
  *   `stream` before its launch, so the SMLA_DEV_* flags of a call cannot be
  *   read back through this entry point.  Calls that overlap on the GPU (other
  *   streams, other host threads) race on the array: order them on one stream.
- * - Otherwise it behaves as smla_decode, including its host checks.
+ * - Every host check of smla_decode runs first, before the array is looked up
+ *   or written; it returns the same status smla_decode would (after the size
+ *   check above).  Otherwise it behaves as smla_decode.
  */
 smla_status smla_decode_static_scratch(const smla_decode_args* args, smla_stream_t stream);
 

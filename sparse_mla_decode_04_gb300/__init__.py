@@ -1,7 +1,8 @@
 """GB300 (sm_103a) sparse multi-head latent attention decode.
 
-The compute path is libsmla.so (include/smla.h): a host split planner and one
-persistent-style tcgen05 decode kernel with an in-kernel split merge.  This
+The compute path is libsmla.so (include/smla.h): a host split planner, a
+persistent tcgen05 decode kernel and a GPU-wide merge kernel for rows that the
+in-kernel split plan cuts into several partials.  This
 package is its Python binding: the C entry points under the same names
 (``smla_decode``, ``smla_plan_num_splits``, ...), plus ``Workspace`` and
 ``decode`` helpers that take torch device tensors.  PyTorch supplies device

@@ -1415,10 +1415,10 @@ __global__ void __launch_bounds__(kMergeThreads) smla_merge_kernel(const KParams
 #pragma unroll 4
     for (int i = 0; i < sr; ++i) {
         const float2 mi = __ldcg(ml + i * ml_step);
+        lall += mi.y;
+        if (mi.x == -INFINITY) continue;  // saw no entry: its O is not read
         const float4 x0 = __ldcg(reinterpret_cast<const float4*>(po + i * po_step));
         const float4 x1 = __ldcg(reinterpret_cast<const float4*>(po + i * po_step) + 1);
-        lall += mi.y;
-        if (mi.x == -INFINITY) continue;
         if (mi.x > M) {  // the running maximum grows: rescale what is summed so far
             const float f = M == -INFINITY ? 0.f : exp2f(M - mi.x);
             Z *= f;

@@ -44,6 +44,44 @@ smla_status check_device() {
 
 }  // namespace
 
+namespace smla {
+
+smla_status check_decode_args(const smla_decode_args* a) {
+    if (a == nullptr) return SMLA_ERR_NULL_POINTER;
+    if (a->num_rows < 1 || a->num_rows > SMLA_MAX_ROWS || a->num_heads < 1 || a->num_heads > SMLA_MAX_HEADS ||
+        a->num_splits < 1 || a->num_splits > SMLA_MAX_SPLITS || a->topk < 0 || a->n_main < 0 || a->n_cmp < 0 ||
+        !std::isfinite(a->sm_scale))
+        return SMLA_ERR_BAD_SHAPE;
+    if (a->q_nope == nullptr || a->q_rope == nullptr || a->out == nullptr) return SMLA_ERR_NULL_POINTER;
+    const bool uses_main = a->topk > 0 || a->swa_len != nullptr;
+    if (a->topk > 0 && a->main_idx == nullptr) return SMLA_ERR_NULL_POINTER;
+    if (a->swa_len != nullptr && a->swa_start == nullptr) return SMLA_ERR_NULL_POINTER;
+    if (uses_main && (a->kv_pool == nullptr || a->kv_scales == nullptr)) return SMLA_ERR_NULL_POINTER;
+    if (a->block_table != nullptr && a->pages_per_seq < 1) return SMLA_ERR_BAD_SHAPE;
+    if (a->cmp_len != nullptr && (a->cmp_start == nullptr || a->cmp_pool == nullptr || a->cmp_scales == nullptr))
+        return SMLA_ERR_NULL_POINTER;
+    if (!aligned(a->q_nope, 16) || !aligned(a->q_rope, 16) || !aligned(a->out, 16) ||
+        !aligned(a->kv_pool, 16) || !aligned(a->cmp_pool, 16) || !aligned(a->kv_scales, 8) ||
+        !aligned(a->cmp_scales, 8) || !aligned(a->block_table, 4) || !aligned(a->row_seq, 4) ||
+        !aligned(a->main_idx, 4) || !aligned(a->swa_start, 4) || !aligned(a->swa_len, 4) ||
+        !aligned(a->cmp_start, 4) || !aligned(a->cmp_len, 4) || !aligned(a->sink, 4) ||
+        !aligned(a->lse, 4))
+        return SMLA_ERR_MISALIGNED;
+    return SMLA_OK;
+}
+
+smla_status check_decode_call(const smla_decode_args* a, const void* workspace, size_t ws_bytes) {
+    if (a == nullptr || workspace == nullptr) return SMLA_ERR_NULL_POINTER;
+    const smla_status st = check_decode_args(a);
+    if (st != SMLA_OK) return st;
+    if (!aligned(workspace, 256)) return SMLA_ERR_MISALIGNED;
+    if (ws_bytes < smla_workspace_bytes(a->num_rows, a->num_heads, a->num_splits))
+        return SMLA_ERR_WORKSPACE_TOO_SMALL;
+    return check_device();
+}
+
+}  // namespace smla
+
 extern "C" {
 
 smla_status smla_plan_default_coeffs(smla_plan_coeffs* out) {
@@ -88,30 +126,8 @@ size_t smla_workspace_bytes(int max_rows, int num_heads, int max_splits) {
 }
 
 smla_status smla_decode(const smla_decode_args* a, void* workspace, size_t ws_bytes, smla_stream_t stream) {
-    if (a == nullptr || workspace == nullptr) return SMLA_ERR_NULL_POINTER;
-    if (a->num_rows < 1 || a->num_rows > SMLA_MAX_ROWS || a->num_heads < 1 || a->num_heads > SMLA_MAX_HEADS ||
-        a->num_splits < 1 || a->num_splits > SMLA_MAX_SPLITS || a->topk < 0 || a->n_main < 0 || a->n_cmp < 0 ||
-        !std::isfinite(a->sm_scale))
-        return SMLA_ERR_BAD_SHAPE;
-    if (a->q_nope == nullptr || a->q_rope == nullptr || a->out == nullptr) return SMLA_ERR_NULL_POINTER;
-    const bool uses_main = a->topk > 0 || a->swa_len != nullptr;
-    if (a->topk > 0 && a->main_idx == nullptr) return SMLA_ERR_NULL_POINTER;
-    if (a->swa_len != nullptr && a->swa_start == nullptr) return SMLA_ERR_NULL_POINTER;
-    if (uses_main && (a->kv_pool == nullptr || a->kv_scales == nullptr)) return SMLA_ERR_NULL_POINTER;
-    if (a->block_table != nullptr && a->pages_per_seq < 1) return SMLA_ERR_BAD_SHAPE;
-    if (a->cmp_len != nullptr && (a->cmp_start == nullptr || a->cmp_pool == nullptr || a->cmp_scales == nullptr))
-        return SMLA_ERR_NULL_POINTER;
-    if (!aligned(a->q_nope, 16) || !aligned(a->q_rope, 16) || !aligned(a->out, 16) ||
-        !aligned(a->kv_pool, 16) || !aligned(a->cmp_pool, 16) || !aligned(a->kv_scales, 8) ||
-        !aligned(a->cmp_scales, 8) || !aligned(a->block_table, 4) || !aligned(a->row_seq, 4) ||
-        !aligned(a->main_idx, 4) || !aligned(a->swa_start, 4) || !aligned(a->swa_len, 4) ||
-        !aligned(a->cmp_start, 4) || !aligned(a->cmp_len, 4) || !aligned(a->sink, 4) ||
-        !aligned(a->lse, 4) || !aligned(workspace, 256))
-        return SMLA_ERR_MISALIGNED;
-    if (ws_bytes < smla_workspace_bytes(a->num_rows, a->num_heads, a->num_splits))
-        return SMLA_ERR_WORKSPACE_TOO_SMALL;
-    const smla_status dev = check_device();
-    if (dev != SMLA_OK) return dev;
+    const smla_status st = smla::check_decode_call(a, workspace, ws_bytes);
+    if (st != SMLA_OK) return st;
     return smla::launch_decode(a, workspace, static_cast<cudaStream_t>(stream));
 }
 

@@ -39,6 +39,14 @@ inline WorkspaceLayout workspace_layout(int rows, int heads, int splits) {
     return L;
 }
 
+// Host checks of smla_decode (defined in smla_host.cpp).  check_decode_args
+// covers the argument struct (sizes, NULL and misaligned pointers);
+// check_decode_call adds the workspace (NULL, 256-byte alignment, size) and
+// the device (compute capability 10.3).  Both return the status smla_decode
+// would return, and touch nothing on the device.
+smla_status check_decode_args(const smla_decode_args* a);
+smla_status check_decode_call(const smla_decode_args* a, const void* workspace, size_t ws_bytes);
+
 // Host-validated launch of the decode and merge kernels (defined in smla_decode.cu).
 smla_status launch_decode(const smla_decode_args* args, void* workspace, cudaStream_t stream);
 

@@ -319,3 +319,60 @@ def test_planner_monotone_in_kv_len():
 def test_planner_prefers_one_wave_over_two():
     # 32 rows: s = 2 fills 64 of 76 slots in one wave; s = 3 would need two waves
     assert oracle.plan_num_splits(32, 128, 10327, COEFFS) == 2
+
+
+# ---------------------------------------------------------------------------
+# the cost model's value, pinned by hand-evaluated cases
+# ---------------------------------------------------------------------------
+def _plan_cases():
+    fx = json.load(open(os.path.join(GOLD, "plan_cost_cases.json")))
+    return fx, [dict(c, coeffs=c.get("coeffs", fx["coeffs"])) for c in fx["cases"]]
+
+
+def test_plan_cost_matches_hand_evaluated_cases():
+    _, cases = _plan_cases()
+    for c in cases:
+        got = O.plan_cost(c["s"], c["R"], c["H"], c["kv"], c["coeffs"])
+        assert got == pytest.approx(c["cost"], rel=1e-12, abs=1e-12), c["what"]
+
+
+def test_plan_argmin_matches_hand_evaluated_case():
+    fx, _ = _plan_cases()
+    for c in fx["argmin"]:
+        assert O.plan_num_splits(c["R"], c["H"], c["kv"], fx["coeffs"], c["s_max"]) == c["s"], c["what"]
+
+
+def _cost_mutants():
+    """Plausible mistakes in the cost model, planted in copies of it."""
+    def waves(R, s, co):
+        return -(-(R * s) // int(co["slots"]))
+
+    def no_split_term(s, R, H, kv, co):
+        return waves(R, s, co) * (co["t0"] + co["c_entry"] * float(-(-kv // s)))
+
+    def split_term_without_s(s, R, H, kv, co):
+        c = no_split_term(s, R, H, kv, co)
+        return c + (co["c_byte"] * float(R * H * 512 * 4) + co["c_merge"] if s > 1 else 0.0)
+
+    def floor_kv(s, R, H, kv, co):
+        c = waves(R, s, co) * (co["t0"] + co["c_entry"] * float(kv // s))
+        return c + (co["c_byte"] * float(R * H * 512 * 4 * s) + co["c_merge"] if s > 1 else 0.0)
+
+    def floor_waves(s, R, H, kv, co):
+        c = max(1, (R * s) // int(co["slots"])) * (co["t0"] + co["c_entry"] * float(-(-kv // s)))
+        return c + (co["c_byte"] * float(R * H * 512 * 4 * s) + co["c_merge"] if s > 1 else 0.0)
+
+    def merge_always(s, R, H, kv, co):
+        return no_split_term(s, R, H, kv, co) + co["c_byte"] * float(R * H * 512 * 4 * s) + co["c_merge"]
+
+    return [no_split_term, split_term_without_s, floor_kv, floor_waves, merge_always]
+
+
+@pytest.mark.parametrize("mutant", _cost_mutants(), ids=lambda f: f.__name__)
+def test_negative_control_plan_cost_mistakes_are_caught(mutant):
+    """Each planted mistake disagrees with at least one hand-evaluated case,
+    so the same mistake in the oracle would fail the pin above."""
+    _, cases = _plan_cases()
+    wrong = [c["what"] for c in cases
+             if mutant(c["s"], c["R"], c["H"], c["kv"], c["coeffs"]) != pytest.approx(c["cost"], rel=1e-12)]
+    assert wrong, f"{mutant.__name__} passes every golden case"

@@ -42,19 +42,62 @@ def test_static_scratch_rejects_oversized_calls(smla_lib):
     assert S.smla_decode_static_scratch(S.smla_decode_args(), 0) == S.SMLA_ERR_BAD_SHAPE
 
 
+def test_static_scratch_limit_matches_the_header(smla_lib):
+    # 32 rows x 128 heads (the DeepSeek-V4-like decode) fits at up to 5 splits;
+    # 96 rows never fit at 128 heads, whatever the split count
+    assert S.smla_workspace_bytes(32, 128, 5) <= 48 * 1024 * 1024 < S.smla_workspace_bytes(32, 128, 6)
+    assert S.smla_workspace_bytes(95, 128, 2) <= 48 * 1024 * 1024 < S.smla_workspace_bytes(96, 128, 1)
+
+
+def _small(seed, lens):
+    return I.build_problem(name="noalloc", seq_lens=list(lens), rows=[(i, L) for i, L in enumerate(lens)], H=128,
+                           topk=512, invalid_frac=0.05, swa=128, seed=seed, device="cuda")
+
+
+def _static_call(p, splits):
+    R, H = p.num_rows, p.num_heads
+    out = torch.full((R, H, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((R, H), float("nan"), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    st = S.smla_decode_static_scratch(_args(p, out, lse, splits), stream)
+    assert st == S.SMLA_OK, S.smla_status_string(st)
+    torch.cuda.synchronize()
+    return out, lse
+
+
 @pytest.mark.gpu
 @pytest.mark.parametrize("splits", [1, 3])
 def test_static_scratch_matches_workspace_entry_point(cuda_device, splits):
-    p = I.build_problem(name="noalloc", seq_lens=[9000, 3000, 700], rows=[(0, 9000), (1, 3000), (2, 700)], H=128,
-                        topk=512, invalid_frac=0.05, swa=128, seed=31, device="cuda")
-    R, H = p.num_rows, p.num_heads
+    p = _small(31, (9000, 3000, 700))
     ref_out, ref_lse = smla.decode(p, num_splits=splits)  # existing entry point, caller-owned workspace
     torch.cuda.synchronize()
-    stream = torch.cuda.current_stream().cuda_stream
     for _ in range(2):  # two calls in a row share the array
-        out = torch.full((R, H, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
-        lse = torch.full((R, H), float("nan"), dtype=torch.float32, device="cuda")
-        st = S.smla_decode_static_scratch(_args(p, out, lse, splits), stream)
-        assert st == S.SMLA_OK, S.smla_status_string(st)
-        torch.cuda.synchronize()
+        out, lse = _static_call(p, splits)
+        _close(out, lse, ref_out, ref_lse)
+
+
+@pytest.mark.gpu
+def test_static_scratch_alternating_shapes(cuda_device):
+    """Consecutive calls of different shapes and split counts: each finds the
+    array as the previous, different call left it."""
+    big, one = _small(32, (20000, 9000, 3000)), _small(33, (15000,))
+    refs = {}
+    for name, p, s in (("big", big, 3), ("one", one, 1)):
+        refs[name] = smla.decode(p, num_splits=s)
+    torch.cuda.synchronize()
+    for name, p, s in (("big", big, 3), ("one", one, 1), ("big", big, 3), ("one", one, 1)):
+        out, lse = _static_call(p, s)
+        _close(out, lse, *refs[name])
+
+
+@pytest.mark.gpu
+def test_static_scratch_dsv4_size(cuda_device):
+    """The largest standard workload that fits the array: 32 rows x 128 heads."""
+    p = I.dsv4(device="cuda")
+    s = smla.smla_plan_num_splits(p.num_rows, p.num_heads, p.kv_len_estimate())
+    assert S.smla_workspace_bytes(p.num_rows, p.num_heads, s) <= 48 * 1024 * 1024
+    ref_out, ref_lse = smla.decode(p, num_splits=s)
+    torch.cuda.synchronize()
+    for _ in range(2):
+        out, lse = _static_call(p, s)
         _close(out, lse, ref_out, ref_lse)
