@@ -71,13 +71,11 @@ namespace smla {
 constexpr int kBK = 64;               // entries per tile (QK N, PV K)
 constexpr int kRawBK = 32;            // entries per raw tile (one producer lane each)
 constexpr int kRawPerTile = kBK / kRawBK;
-constexpr int kNSlot = 6;             // slot-ring stages (raw tiles resolved ahead of the dequant)
+constexpr int kNR = 3;                // raw-byte ring stages
 constexpr int kNXO = 2;               // own-dims tile stages
-constexpr int kNXP = 2;               // peer-dims tile stages
 constexpr int kSoftmaxWarps = 4;      // warps 0-3: one thread per head
-constexpr int kProducerWarp0 = 4;     // warps 4-6: producer pw resolves raw tiles q % 3 == pw
-constexpr int kNumProducers = 3;
-static_assert(kNSlot % kNumProducers == 0, "each slot stage has exactly one producer (its phases are waited in order)");
+constexpr int kProducerWarp0 = 4;     // warps 4-6: producer pw owns raw stage pw (tiles g % kNR == pw)
+constexpr int kNumProducers = kNR;    // one per stage: each waits its stage's phases strictly in order
 constexpr int kMmaWarp = 7;
 constexpr int kDequantWarp0 = 8;      // warps 8-15
 constexpr int kNumDequantWarps = 8;
@@ -107,15 +105,16 @@ constexpr float kLoBudget = 1.0f / 512.0f;
 
 constexpr uint32_t kAtomBytes = kBK * 128;                      // one 64-dim atom of a tile: 8 KB
 constexpr uint32_t kHalfBytes = 4 * kAtomBytes;                 // 256 dims of a tile: 32 KB
-constexpr uint32_t kSlotBytes = kRawBK * 16;                    // per raw tile: [32] {entry ptr, scale ptr}
+constexpr uint32_t kRawStageBytes = kRawBK * SMLA_ENTRY_BYTES;  // 18 KB
 
 // Shared-memory layout (offsets from a 1024-byte-aligned base).
 constexpr uint32_t kOffQ = 0;                                      // Q's own dims: [4 atoms][128][128 B]
 constexpr uint32_t kOffXO = kOffQ + 65536;                         // own dims: [kNXO][4 atoms][64][128 B]
-constexpr uint32_t kOffXP = kOffXO + kNXO * kHalfBytes;            // peer dims: [kNXP][4 atoms][64][128 B]
-constexpr uint32_t kOffSlot = kOffXP + kNXP * kHalfBytes;          // [kNSlot][32] {u64 entry ptr, u64 scale ptr}
-constexpr uint32_t kOffSlotMask = kOffSlot + kNSlot * kSlotBytes;  // [kNSlot] u32 valid masks
-constexpr uint32_t kOffXMask = kOffSlotMask + 32;                  // [kNXO][2] u32 valid masks (64 entries)
+constexpr uint32_t kOffXP = kOffXO + kNXO * kHalfBytes;            // peer dims: [4 atoms][64][128 B]
+constexpr uint32_t kOffRaw = kOffXP + kHalfBytes;                  // [kNR][32][576 B]
+constexpr uint32_t kOffRawSc = kOffRaw + kNR * kRawStageBytes;     // [kNR][32] u64 scale codes
+constexpr uint32_t kOffRawMask = kOffRawSc + kNR * kRawBK * 8;     // [kNR] u32 valid masks
+constexpr uint32_t kOffXMask = kOffRawMask + 16;                   // [kNXO][2] u32 valid masks (64 entries)
 constexpr uint32_t kOffXVmax = kOffXMask + kNXO * 8;               // [kNXO][8 dequant warps] f32 max |V| bound
 constexpr uint32_t kOffVote = kOffXVmax + kNXO * 32;               // [2][4 softmax warps] u32 lo-skip votes
 constexpr uint32_t kOffBar = kOffVote + 32;                     // mbarriers
@@ -126,20 +125,19 @@ constexpr uint32_t kOffUnits = kOffMisc + kMiscBytes;           // unit descript
 constexpr uint32_t kSmemUsed = kOffUnits + kMaxUnitsPerPair * 32;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;               // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(kNSlot <= 8, "slot masks");
-// The plan's per-row scratch (tiles[R], prefix[R+1], ...) aliases the X
-// stages during the prologue, before any dequant warp writes them.
-static_assert(4 * (3 * SMLA_MAX_ROWS + 2 * kMaxStreamRanges + 8) <= kNXO * kHalfBytes, "plan scratch fits in the X stages");
+// The plan's per-row scratch (tiles[R], prefix[R+1]) aliases the raw ring
+// during the prologue, before any producer runs.
+static_assert(4 * (3 * SMLA_MAX_ROWS + 2 * kMaxStreamRanges + 8) <= kNR * kRawStageBytes, "plan scratch fits in the raw ring");
 
 // mbarrier indices
 enum : uint32_t {
-    BAR_SLOT_FULL = 0,                     // [kNSlot] producer -> dequant (32 lanes)
-    BAR_SLOT_EMPTY = BAR_SLOT_FULL + kNSlot,  // [kNSlot] dequant -> producer (kNumDequantWarps)
-    BAR_X_FULL = BAR_SLOT_EMPTY + kNSlot,  // [kNXO] own dims written: dequant -> MMA, softmax (kNumDequantWarps)
-    BAR_XP_FULL = BAR_X_FULL + kNXO,       // [kNXP] peer dims written: dequant -> MMA (kNumDequantWarps)
-    BAR_XO_EMPTY = BAR_XP_FULL + kNXP,     // [kNXO] MMA commit after PV (own dims free)
-    BAR_XP_EMPTY = BAR_XO_EMPTY + kNXO,    // [kNXP] MMA commit after QK's peer half (peer dims free)
-    BAR_S_FULL = BAR_XP_EMPTY + kNXP,      // [2] MMA commit after QK
+    BAR_RAW_FULL = 0,                      // [kNR] producer -> dequant (32 async + 1 arrival, tx bytes)
+    BAR_RAW_EMPTY = BAR_RAW_FULL + kNR,    // [kNR] dequant -> producer (kNumDequantWarps)
+    BAR_X_FULL = BAR_RAW_EMPTY + kNR,      // [kNXO] own dims written: dequant -> MMA, softmax (kNumDequantWarps)
+    BAR_XP_FULL = BAR_X_FULL + kNXO,       // peer dims written: dequant -> MMA (kNumDequantWarps)
+    BAR_XO_EMPTY = BAR_XP_FULL + 1,        // [kNXO] MMA commit after PV (own dims free)
+    BAR_XP_EMPTY = BAR_XO_EMPTY + kNXO,    // MMA commit after QK (peer dims free)
+    BAR_S_FULL = BAR_XP_EMPTY + 1,         // [2] MMA commit after QK
     BAR_P_FULL = BAR_S_FULL + 2,           // [2] softmax -> MMA (kSoftmaxWarps)
     BAR_O_DONE = BAR_P_FULL + 2,           // [2] MMA commit after PV(j), on barrier j % 2
     BAR_Q_READY = BAR_O_DONE + 2,          // softmax -> MMA, once per unit (kSoftmaxWarps)
@@ -383,20 +381,11 @@ __device__ __forceinline__ bool softmax_all(bool v) {
 }
 
 // ---------------------------------------------------------------------------
-// role: producer (warp pw resolves raw tiles q % kNumProducers == pw, where q
-// counts this CTA's raw tiles, two per tile; lane = slot).  Slot stage q %
-// kNSlot always belongs to the same producer, which waits its phases strictly
-// in order (a parity wait cannot tell "two phases ahead" from "previous phase
-// done").  A producer writes no tile data: it resolves each slot to the
-// entry's address and its scale bytes' address, starts both on their way
-// into L2, and hands the two pointers to the dequant warps, which load the
-// bytes straight into registers.  Nothing asynchronous targets shared memory,
-// so a warp that gives up leaves nothing in flight.
+// role: producer (warp pw owns raw stage pw: raw tiles q % kNR == pw, where q
+// counts this CTA's raw tiles, two per tile; lane = slot).  A parity wait
+// cannot tell "two phases ahead" from "previous phase done", so each stage
+// has exactly one producer, which waits its phases in order.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void prefetch_l2(const void* p) {
-    asm volatile("prefetch.global.L2 [%0];" :: "l"(p));
-}
-
 __device__ void producer_role(const KParams& p, const Ctx& c, const UnitDesc* units, int n_units, int pw,
                               uint32_t& err) {
     const smla_decode_args& a = p.a;
@@ -414,8 +403,8 @@ __device__ void producer_role(const KParams& p, const Ctx& c, const UnitDesc* un
         const int nst = ceil_div_i(swa_len, kRawBK);
         const int nct = ceil_div_i(cmp_len, kRawBK);
         for (int t = kRawPerTile * d.t_begin; t < kRawPerTile * d.t_end; ++t, ++q) {
-            if ((int)(q % kNumProducers) != pw) continue;
-            const uint32_t st = q % kNSlot, ph = (q / kNSlot) & 1u;
+            if ((int)(q % kNR) != pw) continue;
+            const uint32_t rs = q % kNR, rph = (q / kNR) & 1u;
             // resolve this lane's slot (raw tiles past the row's end stay empty)
             long long phys = -1;
             bool cmp = false;
@@ -450,27 +439,60 @@ __device__ void producer_role(const KParams& p, const Ctx& c, const UnitDesc* un
             if (phys >= 0) {
                 ep = static_cast<const uint8_t*>(cmp ? a.cmp_pool : a.kv_pool) + phys * SMLA_ENTRY_BYTES;
                 sp = static_cast<const uint8_t*>(cmp ? a.cmp_scales : a.kv_scales) + phys * SMLA_SCALE_BYTES;
-                // every 128-byte line of the entry, and its scale bytes
-#pragma unroll
-                for (int b = 0; b < SMLA_ENTRY_BYTES; b += 128) prefetch_l2(ep + b);
-                prefetch_l2(ep + (SMLA_ENTRY_BYTES - 1));
-                prefetch_l2(sp);
             }
             const uint32_t mask = __ballot_sync(0xffffffffu, ep != nullptr);
-            if (!wait_bar_warp(c, bar_addr(c, BAR_SLOT_EMPTY + st), ph ^ 1u)) return;
-            const uint32_t slot = c.sb + kOffSlot + st * kSlotBytes + 16u * (uint32_t)lane;
-            asm volatile("st.shared.v2.u64 [%0], {%1, %2};"
-                         :: "r"(slot), "l"(reinterpret_cast<uint64_t>(ep)), "l"(reinterpret_cast<uint64_t>(sp))
-                         : "memory");
-            if (lane == 0) st_shared_u32(c.sb + kOffSlotMask + st * 4, mask);
-            mbar_arrive_local(bar_addr(c, BAR_SLOT_FULL + st));  // all 32 lanes, each after its own stores
+            // A run of consecutive pool rows in lanes 0..n-1 (compressed entries,
+            // window entries within a page) moves as one bulk copy.  Other tiles
+            // are gathered with 16-byte cp.async (4 lanes per entry, 8 entries
+            // per instruction): 36 instructions per lane instead of 32 bulk
+            // copies queued on the TMA unit.
+            const uint8_t* ep0 = reinterpret_cast<const uint8_t*>(__shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(ep), 0));
+            const int nvalid = __popc(mask);
+            const bool run = (mask == (nvalid == 32 ? 0xffffffffu : (1u << nvalid) - 1u)) &&
+                             __all_sync(0xffffffffu, ep == nullptr || ep == ep0 + (size_t)lane * SMLA_ENTRY_BYTES);
+            // Start the entries' trip from HBM now; the copy into the stage, once
+            // the stage is free, then finds them in L2.
+            if (run) {
+                if (lane == 0 && nvalid > 0) bulk_prefetch_l2(ep0, (uint32_t)nvalid * SMLA_ENTRY_BYTES);
+            } else if (ep != nullptr) {
+                bulk_prefetch_l2(ep, SMLA_ENTRY_BYTES);
+            }
+            if (!wait_bar_warp(c, bar_addr(c, BAR_RAW_EMPTY + rs), rph ^ 1u)) return;
+            const uint32_t full = bar_addr(c, BAR_RAW_FULL + rs);
+            const uint32_t dst = c.sb + kOffRaw + rs * kRawStageBytes;
+            if (run) {
+                if (lane == 0 && nvalid > 0) {
+                    mbar_expect_tx_only(full, (uint32_t)nvalid * SMLA_ENTRY_BYTES);
+                    bulk_g2s(dst, ep0, (uint32_t)nvalid * SMLA_ENTRY_BYTES, full);
+                }
+            } else {
+#pragma unroll 1
+                for (int rnd = 0; rnd < kRawBK / 8; ++rnd) {
+                    const int e = 8 * rnd + (lane >> 2);
+                    const uint8_t* src = reinterpret_cast<const uint8_t*>(
+                        __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(ep), e));
+                    if (src != nullptr) {
+                        const uint32_t d = dst + (uint32_t)e * SMLA_ENTRY_BYTES;
+#pragma unroll
+                        for (int j = 0; j < SMLA_ENTRY_BYTES / 64; ++j) {
+                            const int k = (lane & 3) + 4 * j;  // 16-byte chunk of the entry
+                            cp_async_16(d + 16 * k, src + 16 * k, 16u);
+                        }
+                    }
+                }
+            }
+            if (ep != nullptr) cp_async_8(c.sb + kOffRawSc + (rs * kRawBK + lane) * 8, sp);
+            cp_async_arrive_noinc(full);  // one of the 32 async arrivals
+            if (lane == 0) {
+                st_shared_u32(c.sb + kOffRawMask + rs * 4, mask);
+                mbar_arrive_local(full);  // the 33rd arrival, ordered after the mask store
+            }
         }
     }
 }
 
 // ---------------------------------------------------------------------------
-// role: dequant (8 warps): entry bytes from L2 -> registers -> bf16 swizzled
-// tile halves
+// role: dequant (8 warps): raw ring -> bf16 swizzled tile halves
 // ---------------------------------------------------------------------------
 // A raw tile (32 entries) fills rows [32 k, 32 k + 32) of a tile, k = 0, 1.
 // Its dims split in two sets of 4 atoms: set 0 = fp8 dims 0..255 (atoms
@@ -478,100 +500,54 @@ __device__ void producer_role(const KParams& p, const Ctx& c, const UnitDesc* un
 // An fp8 warp task is 8 entries x 4 chunks of 16 dims of one atom (lane:
 // entry lane/4, chunk lane%4); a RoPE task is 4 entries x 8 chunks (lane:
 // entry lane/8, chunk lane%8).  With these shapes every quarter-warp's
-// swizzled 16-byte stores fall in 8 distinct bank groups.  Per set and raw
-// tile each warp takes:
+// 16-byte raw-ring loads (576-byte entry stride) and swizzled stores fall in 8
+// distinct 16-byte bank groups.  Per set and raw tile each warp takes:
 //   set 0: fp8 (atom dw/4, entry group dw%4) and (atom 2 + dw/4, group dw%4);
 //   set 1: warps 0-3 fp8 (atom 4, group dw) and (atom 6, group dw),
 //          warps 4-7 fp8 (atom 5, group dw-4) and RoPE tasks 2(dw-4), 2(dw-4)+1.
 // A set is written to the 4-atom buffer `dst` (local atom = atom % 4).
-// The lane's chunks of one set: c[0] is its first fp8 chunk; c[1] its second
-// fp8 chunk, or (set 1, warps 4-7) its first RoPE chunk; c[2] its second RoPE
-// chunk.
-struct SetChunks {
-    uint4 c[3];
-};
-
-__device__ __forceinline__ void set_atoms(int set, int dw, int& a0, int& a1, bool& second_fp8) {
-    if (set == 0) { a0 = dw >> 2; a1 = 2 + (dw >> 2); second_fp8 = true; }
-    else { a0 = dw < 4 ? 4 : 5; a1 = 6; second_fp8 = dw < 4; }
-}
-
-__device__ __forceinline__ uint4 ld_global_v4(const uint8_t* p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
-    return v;
-}
-__device__ __forceinline__ uint2 ld_global_v2(const uint8_t* p) {
-    uint2 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
-    return v;
-}
-__device__ __forceinline__ void ld_shared_v2u64(uint32_t addr, uint64_t& a, uint64_t& b) {
-    asm volatile("ld.shared.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "r"(addr) : "memory");
-}
-
-// Entry of slot e of slot stage st (null for an invalid slot).
-__device__ __forceinline__ const uint8_t* slot_entry(const Ctx& c, uint32_t st, int e) {
-    uint64_t ep, sp;
-    ld_shared_v2u64(c.sb + kOffSlot + st * kSlotBytes + 16u * (uint32_t)e, ep, sp);
-    return reinterpret_cast<const uint8_t*>(ep);
-}
-
-// Issue this lane's global loads of one set of the raw tile in slot stage st.
-__device__ __forceinline__ void load_set(const Ctx& c, uint32_t st, int set, int dw, int lane, SetChunks& x) {
-    int a0, a1;
-    bool second_fp8;
-    set_atoms(set, dw, a0, a1, second_fp8);
-    const int ef = 8 * (dw & 3) + (lane >> 2);
-    const uint8_t* ep = slot_entry(c, st, ef);
-    const int kf = lane & 3;
-    x.c[0] = ep ? ld_global_v4(ep + 16 * (4 * a0 + kf)) : make_uint4(0u, 0u, 0u, 0u);
-    if (second_fp8) {
-        x.c[1] = ep ? ld_global_v4(ep + 16 * (4 * a1 + kf)) : make_uint4(0u, 0u, 0u, 0u);
-        x.c[2] = make_uint4(0u, 0u, 0u, 0u);
-    } else {
-        const int kr = lane & 7;
+// Returns, when `bound` is set, a bound on |x| over the values written.
+__device__ __forceinline__ float dequant_set(uint32_t raw, uint32_t rawsc, uint32_t dst, int row0, uint32_t mask,
+                                             int set, int dw, int lane, bool bound) {
+    const int ef = 8 * (dw & 3) + (lane >> 2);  // entry of this warp's fp8 tasks
+    const bool fvalid = (mask >> (ef & 31)) & 1u;
+    int atom[2];
+    if (set == 0) { atom[0] = dw >> 2; atom[1] = 2 + (dw >> 2); }
+    else { atom[0] = dw < 4 ? 4 : 5; atom[1] = 6; }
+    const bool second_fp8 = set == 0 || dw < 4;
+    uint4 v[2];
+    uint32_t code[2];
 #pragma unroll
-        for (int it = 0; it < 2; ++it) {
-            const int er = 4 * (2 * (dw - 4) + it) + (lane >> 3);
-            const uint8_t* rp = slot_entry(c, st, er);
-            x.c[1 + it] = rp ? ld_global_v4(rp + SMLA_NOPE_DIMS + 16 * kr) : make_uint4(0u, 0u, 0u, 0u);
+    for (int it = 0; it < 2; ++it) {
+        const int k = 4 * atom[it] + (lane & 3);
+        v[it] = make_uint4(0u, 0u, 0u, 0u);
+        code[it] = 127u;
+        if (fvalid && (it == 0 || second_fp8)) {
+            v[it] = ld_shared_v4(raw + ef * SMLA_ENTRY_BYTES + 16 * k);
+            code[it] = ld_shared_u8(rawsc + ef * 8 + atom[it]);
         }
     }
-}
+    const bool has_rope = !second_fp8;
+    uint4 rv[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
+    const int kr = lane & 7;
+    int er[2];
+#pragma unroll
+    for (int it = 0; it < 2; ++it) {
+        er[it] = 4 * (2 * (dw - 4) + it) + (lane >> 3);
+        if (has_rope && ((mask >> (er[it] & 31)) & 1u))
+            rv[it] = ld_shared_v4(raw + er[it] * SMLA_ENTRY_BYTES + SMLA_NOPE_DIMS + 16 * kr);
+    }
 
-// The scale codes of this lane's fp8 entry (all 127 for an invalid slot).
-__device__ __forceinline__ uint2 load_codes(const Ctx& c, uint32_t st, int dw, int lane) {
-    const int ef = 8 * (dw & 3) + (lane >> 2);
-    uint64_t ep, sp;
-    ld_shared_v2u64(c.sb + kOffSlot + st * kSlotBytes + 16u * (uint32_t)ef, ep, sp);
-    return ep ? ld_global_v2(reinterpret_cast<const uint8_t*>(sp)) : make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
-}
-
-__device__ __forceinline__ uint32_t code_of(uint2 sc, int atom) {
-    return ((atom < 4 ? sc.x : sc.y) >> (8 * (atom & 3))) & 0xFFu;
-}
-
-// Convert one set of one raw tile (chunks already in registers) and store it.
-// Returns, when `bound` is set, a bound on |x| over the values written.
-__device__ __forceinline__ float store_set(uint32_t dst, int row0, uint2 sc, int set, int dw, int lane,
-                                           const SetChunks& x, bool bound) {
-    int atom[2];
-    bool second_fp8;
-    set_atoms(set, dw, atom[0], atom[1], second_fp8);
-    const int ef = 8 * (dw & 3) + (lane >> 2);
-    const uint32_t code[2] = {code_of(sc, atom[0]), code_of(sc, atom[1])};
-    const int kk = (lane & 3) * 2;
     // straight-line fast path for every chunk; the rare chunks it gets wrong
     // are redone below with the exact conversion
     uint32_t amax = 0u;
     bool bad[2] = {false, false};
+    const int kk = (lane & 3) * 2;
 #pragma unroll
     for (int it = 0; it < 2; ++it) {
         if (it == 1 && !second_fp8) break;
         uint32_t o[8];
-        dequant16_fast(x.c[it], code[it], o);
+        dequant16_fast(v[it], code[it], o);
         const uint32_t am = absmax_bits8(o);
         bad[it] = fast_chunk_bad(code[it], am);
         amax = max(amax, am);
@@ -580,14 +556,11 @@ __device__ __forceinline__ float store_set(uint32_t dst, int row0, uint2 sc, int
         st_shared_v4(d + sw128_offset(row0 + ef, kk + 1), o[4], o[5], o[6], o[7]);
     }
     float vbound = __uint_as_float(amax << 16);
-    if (!second_fp8) {
-        const int kr = lane & 7;
+    if (has_rope) {
 #pragma unroll
         for (int it = 0; it < 2; ++it) {
-            const int er = 4 * (2 * (dw - 4) + it) + (lane >> 3);
-            const uint4 rv = x.c[1 + it];
-            if (bound) vbound = fmaxf(vbound, bf16x8_absmax(rv));
-            st_shared_v4(dst + 3 * kAtomBytes + sw128_offset(row0 + er, kr), rv.x, rv.y, rv.z, rv.w);
+            if (bound) vbound = fmaxf(vbound, bf16x8_absmax(rv[it]));
+            st_shared_v4(dst + 3 * kAtomBytes + sw128_offset(row0 + er[it], kr), rv[it].x, rv[it].y, rv[it].z, rv[it].w);
         }
     }
     if (__any_sync(0xffffffffu, bad[0] || bad[1])) {  // rare: one copy of the exact path
@@ -595,7 +568,7 @@ __device__ __forceinline__ float store_set(uint32_t dst, int row0, uint2 sc, int
         for (int it = 0; it < 2; ++it) {
             const bool b = it == 0 ? bad[0] : bad[1];
             if (!b) continue;
-            const uint4 vv = it == 0 ? x.c[0] : x.c[1];
+            const uint4 vv = it == 0 ? v[0] : v[1];
             const uint32_t cd = it == 0 ? code[0] : code[1];
             const float scale = ue8m0_to_f32(cd);
             uint32_t o[8];
@@ -610,89 +583,54 @@ __device__ __forceinline__ float store_set(uint32_t dst, int row0, uint2 sc, int
     return bound ? vbound : 0.f;
 }
 
-// The loads run a tile ahead of the conversions: while tile g's peer set is
-// converted, its own set is in flight; right after, tile g + 1's peer set is
-// issued, and after tile g's own set, tile g + 1's own set.  A tile's two
-// slot stages are released once both of its sets have been issued.  Tile g
-// (g counts this CTA's tiles over all its units) takes peer stage g % kNXP,
-// announced on XP_FULL once QK(g - kNXP) has read that stage, and own stage
-// g % kNXO, announced on X_FULL (with the valid masks and a bound on |V|)
-// once PV(g - kNXO) has read it.
+// Per tile g, four steps with one call site (the role's code stays small in
+// the instruction cache): the peer set of raw tile 0 and 1 (once QK(g-1) has
+// read the peer buffer), announced on XP_FULL so that QK(g) can start on those
+// dims; then the own set of raw tile 0 and 1 (once PV(g-2) has read the own
+// stage), each raw stage released after its own set; announced on X_FULL.
 __device__ void dequant_role(const Ctx& c, const UnitDesc* units, int n_units, int dw) {
     const int lane = threadIdx.x & 31;
-    const int own_set = (int)c.half, peer_set = 1 - (int)c.half;
-    uint32_t n_tiles = 0;
-    for (int ui = 0; ui < n_units; ++ui) n_tiles += (uint32_t)(units[ui].t_end - units[ui].t_begin);
-    if (n_tiles == 0) return;
-    SetChunks P[kRawPerTile], O[kRawPerTile];
-    uint2 sc[kRawPerTile];
-    uint32_t mask[kRawPerTile];
-    // tile 0: both sets in flight
-#pragma unroll
-    for (int k = 0; k < kRawPerTile; ++k) {
-        const uint32_t st = (uint32_t)k % kNSlot;
-        if (!wait_bar_warp(c, bar_addr(c, BAR_SLOT_FULL + st), 0u)) return;
-        mask[k] = ld_shared_u32(c.sb + kOffSlotMask + st * 4);
-        sc[k] = load_codes(c, st, dw, lane);
-        load_set(c, st, peer_set, dw, lane, P[k]);
-        load_set(c, st, own_set, dw, lane, O[k]);
-        __syncwarp();
-        if (lane == 0) mbar_arrive_local(bar_addr(c, BAR_SLOT_EMPTY + st));
-    }
-    for (uint32_t g = 0; g < n_tiles; ++g) {
-        const uint32_t ps = g % kNXP, xs = g % kNXO;
-        const bool more = g + 1 < n_tiles;
-        // ---- peer set of tile g
-        if (!wait_bar_warp(c, bar_addr(c, BAR_XP_EMPTY + ps), ((g / kNXP) & 1u) ^ 1u)) return;
-#pragma unroll
-        for (int k = 0; k < kRawPerTile; ++k)
-            store_set(c.sb + kOffXP + ps * kHalfBytes, kRawBK * k, sc[k], peer_set, dw, lane, P[k], false);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_local(bar_addr(c, BAR_XP_FULL + ps));
-        // ---- tile g + 1: its slots, its codes and its peer set
-        uint2 sc_n[kRawPerTile];
-        uint32_t mask_n[kRawPerTile];
-        if (more) {
-#pragma unroll
-            for (int k = 0; k < kRawPerTile; ++k) {
-                const uint32_t q = kRawPerTile * (g + 1) + k, st = q % kNSlot;
-                if (!wait_bar_warp(c, bar_addr(c, BAR_SLOT_FULL + st), (q / kNSlot) & 1u)) return;
-                mask_n[k] = ld_shared_u32(c.sb + kOffSlotMask + st * 4);
-                sc_n[k] = load_codes(c, st, dw, lane);
-                load_set(c, st, peer_set, dw, lane, P[k]);
+    uint32_t g = 0;
+    for (int ui = 0; ui < n_units; ++ui) {
+        const int n = units[ui].t_end - units[ui].t_begin;
+        for (int i = 0; i < n; ++i, ++g) {
+            const uint32_t xs = g % kNXO;
+            uint32_t mask0 = 0u, mask1 = 0u;
+            float vbound = 0.f;
+#pragma unroll 1
+            for (int step = 0; step < 2 * kRawPerTile; ++step) {
+                const int k = step & 1;
+                const bool own = step >= kRawPerTile;
+                const uint32_t q = kRawPerTile * g + k;
+                const uint32_t rs = q % kNR;
+                if (!own) {
+                    if (!wait_bar_warp(c, bar_addr(c, BAR_RAW_FULL + rs), (q / kNR) & 1u)) return;
+                    const uint32_t m = ld_shared_u32(c.sb + kOffRawMask + rs * 4);
+                    if (k == 0) mask0 = m; else mask1 = m;
+                    if (k == 0 && !wait_bar_warp(c, bar_addr(c, BAR_XP_EMPTY), (g & 1u) ^ 1u)) return;
+                } else if (k == 0) {
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_local(bar_addr(c, BAR_XP_FULL));
+                    if (!wait_bar_warp(c, bar_addr(c, BAR_XO_EMPTY + xs), ((g / kNXO) & 1u) ^ 1u)) return;
+                }
+                const uint32_t dst = own ? c.sb + kOffXO + xs * kHalfBytes : c.sb + kOffXP;
+                const int set = own ? (int)c.half : 1 - (int)c.half;
+                vbound = fmaxf(vbound, dequant_set(c.sb + kOffRaw + rs * kRawStageBytes, c.sb + kOffRawSc + rs * kRawBK * 8,
+                                                   dst, kRawBK * k, k == 0 ? mask0 : mask1, set, dw, lane, own));
+                if (own) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_local(bar_addr(c, BAR_RAW_EMPTY + rs));
+                }
             }
-        }
-        // ---- own set of tile g
-        if (!wait_bar_warp(c, bar_addr(c, BAR_XO_EMPTY + xs), ((g / kNXO) & 1u) ^ 1u)) return;
-        float vbound = 0.f;
+            if (dw == 0 && lane < kRawPerTile)
+                st_shared_u32(c.sb + kOffXMask + (xs * kRawPerTile + lane) * 4, lane == 0 ? mask0 : mask1);
 #pragma unroll
-        for (int k = 0; k < kRawPerTile; ++k)
-            vbound = fmaxf(vbound, store_set(c.sb + kOffXO + xs * kHalfBytes, kRawBK * k, sc[k], own_set, dw, lane,
-                                             O[k], true));
-        if (dw == 0 && lane < kRawPerTile)
-            st_shared_u32(c.sb + kOffXMask + (xs * kRawPerTile + lane) * 4, lane == 0 ? mask[0] : mask[1]);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) vbound = fmaxf(vbound, __shfl_xor_sync(0xffffffffu, vbound, o));
-        if (lane == 0) st_shared_f32(c.sb + kOffXVmax + (xs * kNumDequantWarps + dw) * 4, vbound);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_local(bar_addr(c, BAR_X_FULL + xs));
-        // ---- tile g + 1's own set; then its slot stages are free
-        if (more) {
-#pragma unroll
-            for (int k = 0; k < kRawPerTile; ++k) {
-                const uint32_t q = kRawPerTile * (g + 1) + k, st = q % kNSlot;
-                load_set(c, st, own_set, dw, lane, O[k]);
-                sc[k] = sc_n[k];
-                mask[k] = mask_n[k];
-            }
+            for (int o = 16; o > 0; o >>= 1) vbound = fmaxf(vbound, __shfl_xor_sync(0xffffffffu, vbound, o));
+            if (lane == 0) st_shared_f32(c.sb + kOffXVmax + (xs * kNumDequantWarps + dw) * 4, vbound);
+            fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) {
-#pragma unroll
-                for (int k = 0; k < kRawPerTile; ++k)
-                    mbar_arrive_local(bar_addr(c, BAR_SLOT_EMPTY + (kRawPerTile * (g + 1) + k) % kNSlot));
-            }
+            if (lane == 0) mbar_arrive_local(bar_addr(c, BAR_X_FULL + xs));
         }
     }
 }
@@ -734,6 +672,7 @@ __device__ __forceinline__ bool issue_pv(const Ctx& c, uint32_t j, bool first_of
 __device__ void mma_role(const Ctx& c, const UnitDesc* units, int n_units) {
     const uint32_t idesc_qk = idesc_bf16_f32(128, kBK, false, false);
     const uint64_t q_desc0 = sdesc_sw128(c.sb + kOffQ, 16, 1024);
+    const uint64_t xp_desc0 = sdesc_sw128(c.sb + kOffXP, 16, 1024);
     uint32_t g = 0;
     bool ok = true;
     for (int ui = 0; ui < n_units && ok; ++ui) {
@@ -742,11 +681,10 @@ __device__ void mma_role(const Ctx& c, const UnitDesc* units, int n_units) {
         tc_fence_after();
         const uint32_t g0 = g;
         for (int i = 0; i < n; ++i, ++g) {
-            const uint32_t xs = g % kNXO, ps = g % kNXP;
-            if (!wait_bar(c, bar_addr(c, BAR_XP_FULL + ps), (g / kNXP) & 1u)) { ok = false; break; }
+            const uint32_t xs = g % kNXO;
+            if (!wait_bar(c, bar_addr(c, BAR_XP_FULL), g & 1u)) { ok = false; break; }
             tc_fence_after();
             const uint64_t xo_desc0 = sdesc_sw128(c.sb + kOffXO + xs * kHalfBytes, 16, 1024);
-            const uint64_t xp_desc0 = sdesc_sw128(c.sb + kOffXP + ps * kHalfBytes, 16, 1024);
             const uint32_t ts = c.tmem + kTmemS + (g & 1u) * kBK;
             bool pv_issued = false;
             // First the peer dims' 16 K steps (Q from TMEM, X from the peer
@@ -770,7 +708,7 @@ __device__ void mma_role(const Ctx& c, const UnitDesc* units, int n_units) {
                                     xo_desc0 + (uint64_t)(((kk >> 2) * kAtomBytes + (kk & 3) * 32) >> 4), idesc_qk, 1u);
                 }
                 if (part == 0) {
-                    mma_commit(bar_addr(c, BAR_XP_EMPTY + ps));
+                    mma_commit(bar_addr(c, BAR_XP_EMPTY));
                     // PV(g-1) goes between the halves when its P is already
                     // there: it then frees the own stage of tile g+1 earlier.
                     if (i > 0 && mbar_test_wait(bar_addr(c, BAR_P_FULL + ((g - 1) & 1u)), ((g - 1) >> 1) & 1u)) {
@@ -787,7 +725,7 @@ __device__ void mma_role(const Ctx& c, const UnitDesc* units, int n_units) {
     }
     // retire every MMA before TMEM is released
     mma_commit(bar_addr(c, BAR_MMA_FINAL));
-    mbar_wait_bounded(bar_addr(c, BAR_MMA_FINAL), 0, kWaitNs);
+    mbar_wait_bounded<false>(bar_addr(c, BAR_MMA_FINAL), 0, kWaitNs);
 }
 
 // ---------------------------------------------------------------------------
@@ -1361,7 +1299,7 @@ __global__ void __launch_bounds__(kThreads, 1) smla_decode_kernel(const KParams 
     c.half = blockIdx.x & 1u;
     volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + kOffMisc);
     c.abort = misc + 1;
-    int* s_tiles = reinterpret_cast<int*>(smem + kOffXO);   // prologue only (aliases the X stages)
+    int* s_tiles = reinterpret_cast<int*>(smem + kOffRaw);  // prologue only
     int* s_prefix = s_tiles + SMLA_MAX_ROWS;                 // [R + 1]
     int* s_cum = s_prefix + SMLA_MAX_ROWS + 1;               // [R + 1]
     int* s_cut = s_cum + SMLA_MAX_ROWS + 1;                  // [Q + 1] stream-plan cuts
@@ -1373,18 +1311,16 @@ __global__ void __launch_bounds__(kThreads, 1) smla_decode_kernel(const KParams 
     uint32_t err = 0;
     if (tid == 0) {
         misc[1] = 0u;
-        for (int i = 0; i < kNSlot; ++i) {
-            mbar_init(bar_addr(c, BAR_SLOT_FULL + i), 32);  // every lane of the producer
-            mbar_init(bar_addr(c, BAR_SLOT_EMPTY + i), kNumDequantWarps);
+        for (int i = 0; i < kNR; ++i) {
+            mbar_init(bar_addr(c, BAR_RAW_FULL + i), 33);  // 32 async (cp.async) + 1 (producer lane 0)
+            mbar_init(bar_addr(c, BAR_RAW_EMPTY + i), kNumDequantWarps);
         }
         for (int i = 0; i < kNXO; ++i) {
             mbar_init(bar_addr(c, BAR_X_FULL + i), kNumDequantWarps);
             mbar_init(bar_addr(c, BAR_XO_EMPTY + i), 1);
         }
-        for (int i = 0; i < kNXP; ++i) {
-            mbar_init(bar_addr(c, BAR_XP_FULL + i), kNumDequantWarps);
-            mbar_init(bar_addr(c, BAR_XP_EMPTY + i), 1);
-        }
+        mbar_init(bar_addr(c, BAR_XP_EMPTY), 1);
+        mbar_init(bar_addr(c, BAR_XP_FULL), kNumDequantWarps);
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar_addr(c, BAR_S_FULL + i), 1);
             mbar_init(bar_addr(c, BAR_P_FULL + i), kSoftmaxWarps);
@@ -1393,9 +1329,7 @@ __global__ void __launch_bounds__(kThreads, 1) smla_decode_kernel(const KParams 
         mbar_init(bar_addr(c, BAR_O_DONE + 1), 1);
         mbar_init(bar_addr(c, BAR_Q_READY), kSoftmaxWarps);
         mbar_init(bar_addr(c, BAR_MMA_FINAL), 1);
-        // the tensor core's commits arrive on these barriers through the async
-        // proxy: their initialisation is released to it before first use
-        fence_mbar_init();
+        fence_mbar_init_cluster();
     }
     if (warp == kMmaWarp) {
         tmem_alloc(c.sb + kOffMisc, kTmemCols);
