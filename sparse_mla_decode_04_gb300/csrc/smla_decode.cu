@@ -137,8 +137,10 @@ enum : uint32_t {
     BAR_XP_FULL = BAR_X_FULL + kNXO,       // peer dims written: dequant -> MMA (kNumDequantWarps)
     BAR_XO_EMPTY = BAR_XP_FULL + 1,        // [kNXO] MMA commit after PV (own dims free)
     BAR_XP_EMPTY = BAR_XO_EMPTY + kNXO,    // MMA commit after QK (peer dims free)
-    BAR_S_FULL = BAR_XP_EMPTY + 1,         // [2] MMA commit after QK
-    BAR_P_FULL = BAR_S_FULL + 2,           // [2] softmax -> MMA (kSoftmaxWarps)
+    BAR_S_FULL = BAR_XP_EMPTY + 1,         // [2] MMA commit after QK's own-dims half
+    BAR_S_PEER = BAR_S_FULL + 2,           // [2] MMA commit after QK's peer-dims half
+    BAR_S_PEER_READ = BAR_S_PEER + 2,      // [2] softmax holds the peer partial: its columns are free (kSoftmaxWarps)
+    BAR_P_FULL = BAR_S_PEER_READ + 2,      // [2] softmax -> MMA (kSoftmaxWarps)
     BAR_O_DONE = BAR_P_FULL + 2,           // [2] MMA commit after PV(j), on barrier j % 2
     BAR_Q_READY = BAR_O_DONE + 2,          // softmax -> MMA, once per unit (kSoftmaxWarps)
     BAR_MMA_FINAL = BAR_Q_READY + 1,       // teardown: all MMAs retired
@@ -665,10 +667,15 @@ __device__ __forceinline__ bool issue_pv(const Ctx& c, uint32_t j, bool first_of
     return true;
 }
 
-// QK(g) then PV(g-1): the tensor pipe runs QK(g) while the softmax works on
-// tile g-1.  K = 512 in 32 steps of 16 dims: dims 0..255 with Q from TMEM,
-// 256..511 with Q from shared memory; the B operand of a step comes from the
-// own or the peer buffer, whichever holds its dims.
+// Per tile g: QK(g)'s peer half, then its own half, then PV(g-1).  K = 512
+// runs as two separate accumulation chains of 256 dims into the same 64
+// columns: the peer dims (Q from TMEM, X from the peer buffer) first; the
+// softmax warps take that partial into registers (S_PEER_READ), and the own
+// dims (Q and X from shared memory) then start a fresh chain in the same
+// columns.  The softmax adds the two partials in fp32.  Two chains of 256
+// halve the accumulation error of one chain of 512 (the tensor core's
+// accumulation is what bounds the logits' precision), and since fp32
+// addition is commutative both CTAs of a pair hold bit-identical scores.
 __device__ void mma_role(const Ctx& c, const UnitDesc* units, int n_units) {
     const uint32_t idesc_qk = idesc_bf16_f32(128, kBK, false, false);
     const uint64_t q_desc0 = sdesc_sw128(c.sb + kOffQ, 16, 1024);
@@ -681,45 +688,30 @@ __device__ void mma_role(const Ctx& c, const UnitDesc* units, int n_units) {
         tc_fence_after();
         const uint32_t g0 = g;
         for (int i = 0; i < n; ++i, ++g) {
-            const uint32_t xs = g % kNXO;
+            const uint32_t xs = g % kNXO, sb = g & 1u;
+            const uint64_t xo_desc0 = sdesc_sw128(c.sb + kOffXO + xs * kHalfBytes, 16, 1024);
+            const uint32_t ts = c.tmem + kTmemS + sb * kBK;
+            // peer half: its columns last held P(g-2), read by PV(g-2), issued before this
             if (!wait_bar(c, bar_addr(c, BAR_XP_FULL), g & 1u)) { ok = false; break; }
             tc_fence_after();
-            const uint64_t xo_desc0 = sdesc_sw128(c.sb + kOffXO + xs * kHalfBytes, 16, 1024);
-            const uint32_t ts = c.tmem + kTmemS + (g & 1u) * kBK;
-            bool pv_issued = false;
-            // First the peer dims' 16 K steps (Q from TMEM, X from the peer
-            // buffer): the dequant writes them first, and their completion frees
-            // the peer buffer for the next tile.  Then the own dims' 16 steps (Q
-            // and X from shared memory).
-#pragma unroll 1
-            for (int part = 0; part < 2; ++part) {
-                if (part == 0) {
 #pragma unroll
-                    for (int kk = 0; kk < 16; ++kk)
-                        mma_bf16_ts(ts, c.tmem + kTmemQ + kk * 8,
-                                    xp_desc0 + (uint64_t)(((kk >> 2) * kAtomBytes + (kk & 3) * 32) >> 4), idesc_qk,
-                                    kk == 0 ? 0u : 1u);
-                } else {
-                    if (!wait_bar(c, bar_addr(c, BAR_X_FULL + xs), (g / kNXO) & 1u)) { ok = false; break; }
-                    tc_fence_after();
+            for (int kk = 0; kk < 16; ++kk)
+                mma_bf16_ts(ts, c.tmem + kTmemQ + kk * 8,
+                            xp_desc0 + (uint64_t)(((kk >> 2) * kAtomBytes + (kk & 3) * 32) >> 4), idesc_qk,
+                            kk == 0 ? 0u : 1u);
+            mma_commit(bar_addr(c, BAR_XP_EMPTY));
+            mma_commit(bar_addr(c, BAR_S_PEER + sb));
+            // own half: a fresh chain once the softmax holds the peer partial
+            if (!wait_bar(c, bar_addr(c, BAR_S_PEER_READ + sb), (g >> 1) & 1u)) { ok = false; break; }
+            if (!wait_bar(c, bar_addr(c, BAR_X_FULL + xs), (g / kNXO) & 1u)) { ok = false; break; }
+            tc_fence_after();
 #pragma unroll
-                    for (int kk = 0; kk < 16; ++kk)
-                        mma_bf16_ss(ts, q_desc0 + (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4),
-                                    xo_desc0 + (uint64_t)(((kk >> 2) * kAtomBytes + (kk & 3) * 32) >> 4), idesc_qk, 1u);
-                }
-                if (part == 0) {
-                    mma_commit(bar_addr(c, BAR_XP_EMPTY));
-                    // PV(g-1) goes between the halves when its P is already
-                    // there: it then frees the own stage of tile g+1 earlier.
-                    if (i > 0 && mbar_test_wait(bar_addr(c, BAR_P_FULL + ((g - 1) & 1u)), ((g - 1) >> 1) & 1u)) {
-                        if (!issue_pv(c, g - 1, (g - 1) == g0)) { ok = false; break; }
-                        pv_issued = true;
-                    }
-                }
-            }
-            if (!ok) break;
-            mma_commit(bar_addr(c, BAR_S_FULL + (g & 1u)));
-            if (i > 0 && !pv_issued && !issue_pv(c, g - 1, (g - 1) == g0)) { ok = false; break; }
+            for (int kk = 0; kk < 16; ++kk)
+                mma_bf16_ss(ts, q_desc0 + (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4),
+                            xo_desc0 + (uint64_t)(((kk >> 2) * kAtomBytes + (kk & 3) * 32) >> 4), idesc_qk,
+                            kk == 0 ? 0u : 1u);
+            mma_commit(bar_addr(c, BAR_S_FULL + sb));
+            if (i > 0 && !issue_pv(c, g - 1, (g - 1) == g0)) { ok = false; break; }
         }
         if (ok && n > 0 && !issue_pv(c, g - 1, (g - 1) == g0)) ok = false;
     }
@@ -835,7 +827,28 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, UnitDesc* units, in
         float m_used = -INFINITY, lsum = 0.f;
         float skipped = 0.f;  // bound on the lo-half contributions skipped so far (units of lsum)
         bool o_init = false;
-        for (int i = 0; i < n; ++i, ++g) {
+        // QK's peer-dims partial of the tile about to be processed (see mma_role):
+        // taken into registers, which frees its columns for the own-dims chain.
+        float peer[kBK];
+        auto take_peer = [&](uint32_t gg) -> bool {
+            const uint32_t sb = gg & 1u;
+            if (!wait_bar_warp(c, bar_addr(c, BAR_S_PEER + sb), (gg >> 1) & 1u)) return false;
+            tc_fence_after();
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                uint32_t v[32];
+                tmem_ld32(c.tmem + kTmemS + sb * kBK + lane_base + 32 * hf, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) peer[32 * hf + j] = __uint_as_float(v[j]);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_local(bar_addr(c, BAR_S_PEER_READ + sb));
+            return true;
+        };
+        if (n > 0 && !take_peer(g)) ok = false;
+        for (int i = 0; i < n && ok; ++i, ++g) {
             const uint32_t sbuf = g & 1u;
             const uint32_t ts = c.tmem + kTmemS + sbuf * kBK + lane_base;
             if (!wait_bar_warp(c, bar_addr(c, BAR_S_FULL + sbuf), (g >> 1) & 1u)) { ok = false; break; }
@@ -847,14 +860,17 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, UnitDesc* units, in
             const uint32_t xs = g % kNXO;
             const uint32_t vmask0 = ld_shared_u32(c.sb + kOffXMask + (xs * kRawPerTile) * 4);
             const uint32_t vmask1 = ld_shared_u32(c.sb + kOffXMask + (xs * kRawPerTile + 1) * 4);
-            // pass 1: the tile's masked maximum (scores are reloaded in pass 2, so
-            // only 32 of them are live at a time)
+            // pass 1: the scores (own-dims chain + peer-dims partial, added in
+            // fp32 and written back for pass 2) and the tile's masked maximum
             float mt = -INFINITY;
-#pragma unroll 1
+#pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
                 uint32_t v[32];
                 tmem_ld32(ts + 32 * hf, v);
                 tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) + peer[32 * hf + j]);
+                tmem_st32(ts + 32 * hf, v);
                 const uint32_t vm = hf == 0 ? vmask0 : vmask1;
                 float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
@@ -862,6 +878,7 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, UnitDesc* units, in
                     mx[j & 3] = fmaxf(mx[j & 3], ((vm >> j) & 1u) ? __uint_as_float(v[j]) * qscale : -INFINITY);
                 mt = fmaxf(mt, fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])));
             }
+            tmem_wait_st();  // pass 2 reloads the sums
             float m_new = m_used;
             if (m_used == -INFINITY || mt > m_used + kRescaleThreshold) m_new = fmaxf(m_used, mt);
             const float alpha = (m_used == -INFINITY) ? 0.f : ex2_approx(m_used - m_new);
@@ -957,6 +974,7 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, UnitDesc* units, in
             __syncwarp();
             if (lane == 0) mbar_arrive_local(bar_addr(c, BAR_P_FULL + sbuf));
             o_init = true;
+            if (i + 1 < n && !take_peer(g + 1)) { ok = false; break; }
         }
         if (ok && n > 0) {  // the unit's last PV (PV(g-1)); earlier ones retired before it
             if (!wait_bar_warp(c, bar_addr(c, BAR_O_DONE + ((g - 1) & 1u)), ((g - 1) >> 1) & 1u)) ok = false;
@@ -1323,6 +1341,8 @@ __global__ void __launch_bounds__(kThreads, 1) smla_decode_kernel(const KParams 
         mbar_init(bar_addr(c, BAR_XP_FULL), kNumDequantWarps);
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar_addr(c, BAR_S_FULL + i), 1);
+            mbar_init(bar_addr(c, BAR_S_PEER + i), 1);
+            mbar_init(bar_addr(c, BAR_S_PEER_READ + i), kSoftmaxWarps);
             mbar_init(bar_addr(c, BAR_P_FULL + i), kSoftmaxWarps);
         }
         mbar_init(bar_addr(c, BAR_O_DONE), 1);
