@@ -97,7 +97,10 @@ constexpr uint32_t kTmemQ = 384;      // Q's peer dims, bf16 packed: [384, 512)
 constexpr uint64_t kWaitNs = 2000000000ull;  // bounded-wait limit (2 s)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units: P may grow to 2^8 before O is rescaled
+// log2 units: P may grow to 2^32 before O is rescaled.  O then stays below
+// n * 2^32 * max|x|, far inside fp32's range for any row length and scale
+// codes up to about 190, and the (TMEM-heavy) rescale of O becomes rare.
+constexpr float kRescaleThreshold = 32.0f;
 // The lo half of P is skipped on a tile only while, for every head, the bound
 // on everything skipped so far stays within kLoBudget of the running softmax
 // denominator: the output error from skipping is then at most kLoBudget.
@@ -861,7 +864,9 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, UnitDesc* units, in
             const uint32_t vmask0 = ld_shared_u32(c.sb + kOffXMask + (xs * kRawPerTile) * 4);
             const uint32_t vmask1 = ld_shared_u32(c.sb + kOffXMask + (xs * kRawPerTile + 1) * 4);
             // pass 1: the scores (own-dims chain + peer-dims partial, added in
-            // fp32 and written back for pass 2) and the tile's masked maximum
+            // fp32 and written back for pass 2) and the tile's masked maximum.
+            // The maximum is taken over the raw scores and scaled once
+            // (qscale > 0); a fully valid half skips the per-entry mask test.
             float mt = -INFINITY;
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
@@ -873,11 +878,17 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, UnitDesc* units, in
                 tmem_st32(ts + 32 * hf, v);
                 const uint32_t vm = hf == 0 ? vmask0 : vmask1;
                 float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                if (vm == 0xffffffffu) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    mx[j & 3] = fmaxf(mx[j & 3], ((vm >> j) & 1u) ? __uint_as_float(v[j]) * qscale : -INFINITY);
+                    for (int j = 0; j < 32; ++j) mx[j & 3] = fmaxf(mx[j & 3], __uint_as_float(v[j]));
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        mx[j & 3] = fmaxf(mx[j & 3], ((vm >> j) & 1u) ? __uint_as_float(v[j]) : -INFINITY);
+                }
                 mt = fmaxf(mt, fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])));
             }
+            mt *= qscale;
             tmem_wait_st();  // pass 2 reloads the sums
             float m_new = m_used;
             if (m_used == -INFINITY || mt > m_used + kRescaleThreshold) m_new = fmaxf(m_used, mt);
@@ -899,11 +910,11 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, UnitDesc* units, in
                                                    : 64.f * ex2_approx(mt - msub) * (1.0f / 512.0f) * (1.0f + 1.0f / 256.0f);
             const bool cold = __all_sync(0xffffffffu, (h >= H) || (skipped * alpha + lo_cap * vmax <= kLoBudget * lsum * alpha));
             // ---- pass 2: P = 2^(s - m) as a bf16 pair hi = bf16(p), lo = bf16(p - hi),
-            // written back over the scores one 16-entry step at a time: entries
-            // 16 q .. 16 q + 15 (columns [16 q, 16 q + 16)) become hi in columns
-            // [16 q, 16 q + 8) and lo in [16 q + 8, 16 q + 16).  Safe before PV(g-1)
-            // completes: these columns were last read by PV(g-2), which retired
-            // before QK(g) (same issue stream) produced this tile's scores.
+            // written over the scores' columns one 16-entry step at a time:
+            // entries 16 q .. 16 q + 15 become hi in columns [16 q, 16 q + 8) and
+            // lo in [16 q + 8, 16 q + 16).  Safe before PV(g-1) completes: these
+            // columns were last read by PV(g-2), which retired before QK(g) (same
+            // issue stream) produced this tile's scores.
             float ps = 0.f, lo_abs = 0.f;
             {
                 float sm[4] = {0.f, 0.f, 0.f, 0.f}, la[4] = {0.f, 0.f, 0.f, 0.f};
@@ -913,25 +924,28 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, UnitDesc* units, in
                     tmem_ld16(ts + 16 * q, v);
                     tmem_wait_ld();
                     const uint32_t vm = ((q < 2 ? vmask0 : vmask1) >> (16 * (q & 1))) & 0xFFFFu;
-                    uint32_t hv[8], lv[8];
+                    uint32_t hl[16];  // hi pairs, then lo pairs
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
-                        const float x0 = ((vm >> (2 * j)) & 1u) ? fmaf(__uint_as_float(v[2 * j]), qscale, -msub) : -INFINITY;
-                        const float x1 = ((vm >> (2 * j + 1)) & 1u) ? fmaf(__uint_as_float(v[2 * j + 1]), qscale, -msub) : -INFINITY;
+                        float x0 = fmaf(__uint_as_float(v[2 * j]), qscale, -msub);
+                        float x1 = fmaf(__uint_as_float(v[2 * j + 1]), qscale, -msub);
+                        if (vm != 0xFFFFu) {
+                            x0 = ((vm >> (2 * j)) & 1u) ? x0 : -INFINITY;
+                            x1 = ((vm >> (2 * j + 1)) & 1u) ? x1 : -INFINITY;
+                        }
                         const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
                         sm[j & 3] += p0 + p1;
                         const __nv_bfloat162 hb = __floats2bfloat162_rn(p0, p1);
-                        memcpy(&hv[j], &hb, 4);
+                        memcpy(&hl[j], &hb, 4);
                         if (cold) {
-                            lv[j] = 0u;
+                            hl[8 + j] = 0u;
                         } else {
                             const float r0 = p0 - __low2float(hb), r1 = p1 - __high2float(hb);
-                            lv[j] = pack_bf16(r0, r1);
+                            hl[8 + j] = pack_bf16(r0, r1);
                             la[j & 3] += fabsf(r0) + fabsf(r1);
                         }
                     }
-                    tmem_st8(ts + 16 * q, hv);
-                    tmem_st8(ts + 16 * q + 8, lv);
+                    tmem_st16(ts + 16 * q, hl);
                 }
                 ps = (sm[0] + sm[1]) + (sm[2] + sm[3]);
                 // |bf16(r)| <= |r| (1 + 2^-8): a bound on the sum of |lo|
