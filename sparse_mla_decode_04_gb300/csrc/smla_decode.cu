@@ -73,16 +73,20 @@ constexpr int kRawBK = 32;            // entries per raw tile (one producer lane
 constexpr int kRawPerTile = kBK / kRawBK;
 constexpr int kNR = 3;                // raw-byte ring stages
 constexpr int kNXO = 2;               // own-dims tile stages
-constexpr int kSoftmaxWarps = 4;      // warps 0-3: one thread per head
-constexpr int kProducerWarp0 = 4;     // warps 4-6: producer pw owns raw stage pw (tiles g % kNR == pw)
+// Softmax warps 0-7: warp w serves heads 32 (w % 4) .. 32 (w % 4) + 31 (TMEM
+// lanes, one thread per head) and side w / 4 of each tile: entries
+// 32 (w / 4) .. 32 (w / 4) + 31.  Side 0 also stages Q and finishes units.
+constexpr int kSoftmaxWarps = 8;
+constexpr int kSideWarps = 4;
+constexpr int kProducerWarp0 = 8;     // warps 8-10: producer pw owns raw stage pw (tiles g % kNR == pw)
 constexpr int kNumProducers = kNR;    // one per stage: each waits its stage's phases strictly in order
-constexpr int kMmaWarp = 7;
-constexpr int kDequantWarp0 = 8;      // warps 8-15
+constexpr int kMmaWarp = 11;
+constexpr int kDequantWarp0 = 12;     // warps 12-19
 constexpr int kNumDequantWarps = 8;
-constexpr int kWarps = 16;
+constexpr int kWarps = 20;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kHeadsPad = 128;        // heads padded up to the MMA M
-static_assert(kHeadsPad == 32 * kSoftmaxWarps, "one softmax thread per padded head");
+static_assert(kHeadsPad == 32 * kSideWarps, "one softmax thread per padded head on each side");
 static_assert(kRawBK == 32, "one producer lane per slot");
 constexpr int kMaxUnitsPerPair = 32;
 constexpr int kUnitCostTiles = 2;     // plan estimate: staging + finishing a unit, in tiles
@@ -119,8 +123,9 @@ constexpr uint32_t kOffRawSc = kOffRaw + kNR * kRawStageBytes;     // [kNR][32] 
 constexpr uint32_t kOffRawMask = kOffRawSc + kNR * kRawBK * 8;     // [kNR] u32 valid masks
 constexpr uint32_t kOffXMask = kOffRawMask + 16;                   // [kNXO][2] u32 valid masks (64 entries)
 constexpr uint32_t kOffXVmax = kOffXMask + kNXO * 8;               // [kNXO][8 dequant warps] f32 max |V| bound
-constexpr uint32_t kOffVote = kOffXVmax + kNXO * 32;               // [2][4 softmax warps] u32 lo-skip votes
-constexpr uint32_t kOffBar = kOffVote + 32;                     // mbarriers
+constexpr uint32_t kOffVote = kOffXVmax + kNXO * 32;               // [2][4 head quarters] u32 lo-skip votes
+constexpr uint32_t kOffXch = kOffVote + 32;                        // [3][2 sides][128 heads] f32 side exchange
+constexpr uint32_t kOffBar = kOffXch + 3 * 2 * 128 * 4;         // mbarriers
 constexpr uint32_t kNumBars = 32;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;           // tmem base, flags, reductions
 constexpr uint32_t kMiscBytes = 512;
@@ -145,7 +150,7 @@ enum : uint32_t {
     BAR_S_PEER_READ = BAR_S_PEER + 2,      // [2] softmax holds the peer partial: its columns are free (kSoftmaxWarps)
     BAR_P_FULL = BAR_S_PEER_READ + 2,      // [2] softmax -> MMA (kSoftmaxWarps)
     BAR_O_DONE = BAR_P_FULL + 2,           // [2] MMA commit after PV(j), on barrier j % 2
-    BAR_Q_READY = BAR_O_DONE + 2,          // softmax -> MMA, once per unit (kSoftmaxWarps)
+    BAR_Q_READY = BAR_O_DONE + 2,          // side-0 softmax -> MMA, once per unit (kSideWarps)
     BAR_MMA_FINAL = BAR_Q_READY + 1,       // teardown: all MMAs retired
     BAR_COUNT = BAR_MMA_FINAL + 1
 };
@@ -368,22 +373,29 @@ __device__ __forceinline__ uint32_t ld_shared_u8(uint32_t addr) {
     return v;
 }
 
-// Named barrier over the softmax warps only (id 1; id 0 is __syncthreads).
-__device__ __forceinline__ void softmax_bar() {
-    asm volatile("bar.sync 1, %0;" :: "r"(kSoftmaxWarps * 32) : "memory");
+// Named barriers (id 0 is __syncthreads): 1 = all softmax warps, 2..5 = the
+// two warps of a head quarter, 6 = the side-0 softmax warps.  Every softmax
+// warp runs the same sequence of them (no early exit between two of them),
+// so none can be left waiting.
+__device__ __forceinline__ void side0_bar() {
+    asm volatile("bar.sync 6, %0;" :: "r"(kSideWarps * 32) : "memory");
 }
 
-// AND of `v` over the softmax warps (named barrier 1): every softmax thread
-// reaches it exactly once per unit, whatever happened in the tile loop.
-__device__ __forceinline__ bool softmax_all(bool v) {
+// AND of `v` over the threads of named barrier `id` (`count` threads).
+__device__ __forceinline__ bool bar_all(uint32_t id, uint32_t count, bool v) {
     uint32_t r;
     asm volatile("{\n\t.reg .pred p, q;\n\t"
                  "setp.ne.u32 p, %1, 0;\n\t"
-                 "bar.red.and.pred q, 1, %2, p;\n\t"
+                 "bar.red.and.pred q, %2, %3, p;\n\t"
                  "selp.u32 %0, 1, 0, q;\n\t}"
-                 : "=r"(r) : "r"((uint32_t)v), "r"(kSoftmaxWarps * 32) : "memory");
+                 : "=r"(r) : "r"((uint32_t)v), "r"(id), "r"(count) : "memory");
     return r != 0u;
 }
+// AND over all softmax warps: every softmax thread reaches it once per unit.
+__device__ __forceinline__ bool softmax_all(bool v) { return bar_all(1u, kSoftmaxWarps * 32, v); }
+// AND over the two warps of head quarter qw (the values of both sides are
+// exchanged through shared memory around it).
+__device__ __forceinline__ bool pair_all(int qw, bool v) { return bar_all(2u + (uint32_t)qw, 64u, v); }
 
 // ---------------------------------------------------------------------------
 // role: producer (warp pw owns raw stage pw: raw tiles q % kNR == pw, where q
@@ -659,7 +671,7 @@ __device__ __forceinline__ bool issue_pv(const Ctx& c, uint32_t j, bool first_of
                     (first_of_unit && kk == 0) ? 0u : 1u);
     uint32_t votes = 1u;
 #pragma unroll
-    for (int w = 0; w < kSoftmaxWarps; ++w) votes &= ld_shared_u32(c.sb + kOffVote + (sb * 4 + w) * 4);
+    for (int w = 0; w < kSideWarps; ++w) votes &= ld_shared_u32(c.sb + kOffVote + (sb * 4 + w) * 4);
     if (votes == 0u) {  // some head needs the lo half of P on this tile
 #pragma unroll
         for (int kk = 0; kk < kBK / 16; ++kk)
@@ -754,11 +766,13 @@ __device__ __forceinline__ void stage_flush(const Ctx& c, int warp, int lane, in
 // ---------------------------------------------------------------------------
 __device__ void softmax_role(const KParams& p, const Ctx& c, UnitDesc* units, int n_units, uint32_t& err) {
     const smla_decode_args& a = p.a;
-    const int h = threadIdx.x;  // 0..127
-    const int warp = threadIdx.x >> 5;
+    const int warp = threadIdx.x >> 5;     // 0..7
     const int lane = threadIdx.x & 31;
+    const int qw = warp & 3;               // head quarter (TMEM lanes 32 qw ..)
+    const int sd = warp >> 2;              // side: tile entries 32 sd .. 32 sd + 31
+    const int h = 32 * qw + lane;          // head (TMEM lane) of this thread
     const int H = a.num_heads;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t lane_base = (uint32_t)(qw * 32) << 16;
     const float qscale = a.sm_scale * kLog2e;
     const float sink2 = (a.sink != nullptr && h < H) ? __ldg(a.sink + h) * kLog2e : -INFINITY;
     uint32_t g = 0;
@@ -768,11 +782,11 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, UnitDesc* units, in
         const UnitDesc d = units[ui];
         const int r = d.row;
         const int n = d.t_end - d.t_begin;
-        // ---- Q of this row: its peer dims (the 256 this CTA does not output)
-        //      -> TMEM [384, 512) as bf16 pairs, its own dims -> shared memory,
-        //      K-major with the 128-byte swizzle.  The next unit's q rows are
-        //      prefetched into L2 now, a unit ahead.
-        {
+        // ---- Q of this row (side 0): its peer dims (the 256 this CTA does not
+        //      output) -> TMEM [384, 512) as bf16 pairs, its own dims -> shared
+        //      memory, K-major with the 128-byte swizzle.  The next unit's q rows
+        //      are prefetched into L2 now, a unit ahead.
+        if (sd == 0) {
             if (h == 0 && ui + 1 < n_units) {
                 const size_t rn = (size_t)units[ui + 1].row * H;
                 bulk_prefetch_l2(static_cast<const uint16_t*>(a.q_nope) + rn * SMLA_NOPE_DIMS,
@@ -817,7 +831,7 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, UnitDesc* units, in
                         }
                         tmem_st32(c.tmem + kTmemQ + lane_base + 32 * hc, v);
                     }
-                    softmax_bar();  // all staged rows read before the own dims overwrite the region
+                    side0_bar();  // all staged rows read before the own dims overwrite the region
                 }
             }
             fence_proxy_async_smem();
@@ -830,53 +844,53 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, UnitDesc* units, in
         float m_used = -INFINITY, lsum = 0.f;
         float skipped = 0.f;  // bound on the lo-half contributions skipped so far (units of lsum)
         bool o_init = false;
-        // QK's peer-dims partial of the tile about to be processed (see mma_role):
-        // taken into registers, which frees its columns for the own-dims chain.
-        float peer[kBK];
+        // QK's peer-dims partial of this side's 32 columns of the tile about to
+        // be processed (see mma_role): taken into registers, which frees the
+        // columns for the own-dims chain.
+        float peer[32];
         auto take_peer = [&](uint32_t gg) -> bool {
             const uint32_t sb = gg & 1u;
             if (!wait_bar_warp(c, bar_addr(c, BAR_S_PEER + sb), (gg >> 1) & 1u)) return false;
             tc_fence_after();
+            uint32_t v[32];
+            tmem_ld32(c.tmem + kTmemS + sb * kBK + lane_base + 32 * sd, v);
+            tmem_wait_ld();
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                uint32_t v[32];
-                tmem_ld32(c.tmem + kTmemS + sb * kBK + lane_base + 32 * hf, v);
-                tmem_wait_ld();
-#pragma unroll
-                for (int j = 0; j < 32; ++j) peer[32 * hf + j] = __uint_as_float(v[j]);
-            }
+            for (int j = 0; j < 32; ++j) peer[j] = __uint_as_float(v[j]);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_local(bar_addr(c, BAR_S_PEER_READ + sb));
             return true;
         };
-        if (n > 0 && !take_peer(g)) ok = false;
-        for (int i = 0; i < n && ok; ++i, ++g) {
+        // Both warps of a head quarter hold the same per-head state (m_used,
+        // lsum, skipped), exchanged twice per tile through kOffXch; every warp
+        // runs every tile's two exchanges even after a failed wait, so the
+        // pair barriers always match.
+        const uint32_t xch = c.sb + kOffXch;
+        auto xch_addr = [&](int k, int side) { return xch + (uint32_t)((k * 2 + side) * 128 + h) * 4u; };
+        if (n > 0 && ok) ok = take_peer(g);
+        for (int i = 0; i < n; ++i, ++g) {
             const uint32_t sbuf = g & 1u;
-            const uint32_t ts = c.tmem + kTmemS + sbuf * kBK + lane_base;
-            if (!wait_bar_warp(c, bar_addr(c, BAR_S_FULL + sbuf), (g >> 1) & 1u)) { ok = false; break; }
+            const uint32_t ts = c.tmem + kTmemS + sbuf * kBK + lane_base + 32 * sd;  // this side's 32 columns
+            const uint32_t xs = g % kNXO;
             // The tile's valid mask and |V| bound were written before its X_FULL
             // arrival; X_FULL of this tile cannot have advanced further (its stage
             // is refilled only after PV of this tile, which needs this thread's P).
-            if (!wait_bar_warp(c, bar_addr(c, BAR_X_FULL + g % kNXO), (g / kNXO) & 1u)) { ok = false; break; }
+            if (ok && !wait_bar_warp(c, bar_addr(c, BAR_S_FULL + sbuf), (g >> 1) & 1u)) ok = false;
+            if (ok && !wait_bar_warp(c, bar_addr(c, BAR_X_FULL + xs), (g / kNXO) & 1u)) ok = false;
             tc_fence_after();
-            const uint32_t xs = g % kNXO;
-            const uint32_t vmask0 = ld_shared_u32(c.sb + kOffXMask + (xs * kRawPerTile) * 4);
-            const uint32_t vmask1 = ld_shared_u32(c.sb + kOffXMask + (xs * kRawPerTile + 1) * 4);
-            // pass 1: the scores (own-dims chain + peer-dims partial, added in
-            // fp32 and written back for pass 2) and the tile's masked maximum.
-            // The maximum is taken over the raw scores and scaled once
-            // (qscale > 0); a fully valid half skips the per-entry mask test.
-            float mt = -INFINITY;
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
+            const uint32_t vm = ld_shared_u32(c.sb + kOffXMask + (xs * kRawPerTile + sd) * 4);
+            // pass 1: this side's scores (own-dims chain + peer-dims partial, added
+            // in fp32 and written back for pass 2) and their masked maximum (taken
+            // over the raw scores: qscale > 0)
+            float mts = -INFINITY;
+            if (ok) {
                 uint32_t v[32];
-                tmem_ld32(ts + 32 * hf, v);
+                tmem_ld32(ts, v);
                 tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) + peer[32 * hf + j]);
-                tmem_st32(ts + 32 * hf, v);
-                const uint32_t vm = hf == 0 ? vmask0 : vmask1;
+                for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) + peer[j]);
+                tmem_st32(ts, v);
                 float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
                 if (vm == 0xffffffffu) {
 #pragma unroll
@@ -886,10 +900,13 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, UnitDesc* units, in
                     for (int j = 0; j < 32; ++j)
                         mx[j & 3] = fmaxf(mx[j & 3], ((vm >> j) & 1u) ? __uint_as_float(v[j]) : -INFINITY);
                 }
-                mt = fmaxf(mt, fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])));
+                mts = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+                tmem_wait_st();  // pass 2 reloads the sums
             }
-            mt *= qscale;
-            tmem_wait_st();  // pass 2 reloads the sums
+            st_shared_f32(xch_addr(0, sd), mts);
+            ok = pair_all(qw, ok);
+            const float mt0 = ld_shared_f32(xch_addr(0, 0)) * qscale, mt1 = ld_shared_f32(xch_addr(0, 1)) * qscale;
+            const float mt = fmaxf(mt0, mt1);
             float m_new = m_used;
             if (m_used == -INFINITY || mt > m_used + kRescaleThreshold) m_new = fmaxf(m_used, mt);
             const float alpha = (m_used == -INFINITY) ? 0.f : ex2_approx(m_used - m_new);
@@ -897,41 +914,43 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, UnitDesc* units, in
             const float msub = (m_new == -INFINITY) ? 0.f : m_new;
             const bool rescale = o_init && (m_new != m_used);
             m_used = m_new;
-            // A cold tile: for every head of this warp, dropping the tile's whole
-            // lo half keeps the skipped total within the budget on the bound
-            // alone (p <= 2^(mt - m) per entry, |lo| <= p 2^-9 by bf16 rounding,
-            // and the new denominator is at least lsum alpha).  Then lo is not
-            // computed: it is stored as 0 and that bound stands in for its sum.
+            // A cold tile: for every head of this quarter, dropping the tile's
+            // whole lo half keeps the skipped total within the budget on the bound
+            // alone (p <= 2^(mt_side - m) per entry, |lo| <= p 2^-9 by bf16
+            // rounding, and the new denominator is at least lsum alpha).  Then lo
+            // is not computed: it is stored as 0 and that bound stands in for its
+            // sum.  Both sides take the same decision from the same values.
             const uint32_t vb = c.sb + kOffXVmax + xs * (4 * kNumDequantWarps);
             float vmax = ld_shared_f32(vb);
 #pragma unroll
             for (int w = 1; w < kNumDequantWarps; ++w) vmax = fmaxf(vmax, ld_shared_f32(vb + 4 * w));
-            const float lo_cap = (mt == -INFINITY) ? 0.f
-                                                   : 64.f * ex2_approx(mt - msub) * (1.0f / 512.0f) * (1.0f + 1.0f / 256.0f);
-            const bool cold = __all_sync(0xffffffffu, (h >= H) || (skipped * alpha + lo_cap * vmax <= kLoBudget * lsum * alpha));
+            const float capk = 32.f * (1.0f / 512.0f) * (1.0f + 1.0f / 256.0f);
+            const float cap0 = mt0 == -INFINITY ? 0.f : capk * ex2_approx(mt0 - msub);
+            const float cap1 = mt1 == -INFINITY ? 0.f : capk * ex2_approx(mt1 - msub);
+            const bool cold = __all_sync(0xffffffffu, (h >= H) || (skipped * alpha + (cap0 + cap1) * vmax <= kLoBudget * lsum * alpha));
             // ---- pass 2: P = 2^(s - m) as a bf16 pair hi = bf16(p), lo = bf16(p - hi),
-            // written over the scores' columns one 16-entry step at a time:
+            // written over this side's columns one 16-entry step at a time:
             // entries 16 q .. 16 q + 15 become hi in columns [16 q, 16 q + 8) and
             // lo in [16 q + 8, 16 q + 16).  Safe before PV(g-1) completes: these
             // columns were last read by PV(g-2), which retired before QK(g) (same
             // issue stream) produced this tile's scores.
-            float ps = 0.f, lo_abs = 0.f;
-            {
+            float ps_side = 0.f, lo_side = 0.f;
+            if (ok) {
                 float sm[4] = {0.f, 0.f, 0.f, 0.f}, la[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
-                for (int q = 0; q < kBK / 16; ++q) {
+                for (int q = 0; q < 2; ++q) {
                     uint32_t v[16];
                     tmem_ld16(ts + 16 * q, v);
                     tmem_wait_ld();
-                    const uint32_t vm = ((q < 2 ? vmask0 : vmask1) >> (16 * (q & 1))) & 0xFFFFu;
+                    const uint32_t vq = (vm >> (16 * q)) & 0xFFFFu;
                     uint32_t hl[16];  // hi pairs, then lo pairs
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         float x0 = fmaf(__uint_as_float(v[2 * j]), qscale, -msub);
                         float x1 = fmaf(__uint_as_float(v[2 * j + 1]), qscale, -msub);
-                        if (vm != 0xFFFFu) {
-                            x0 = ((vm >> (2 * j)) & 1u) ? x0 : -INFINITY;
-                            x1 = ((vm >> (2 * j + 1)) & 1u) ? x1 : -INFINITY;
+                        if (vq != 0xFFFFu) {
+                            x0 = ((vq >> (2 * j)) & 1u) ? x0 : -INFINITY;
+                            x1 = ((vq >> (2 * j + 1)) & 1u) ? x1 : -INFINITY;
                         }
                         const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
                         sm[j & 3] += p0 + p1;
@@ -947,48 +966,56 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, UnitDesc* units, in
                     }
                     tmem_st16(ts + 16 * q, hl);
                 }
-                ps = (sm[0] + sm[1]) + (sm[2] + sm[3]);
+                ps_side = (sm[0] + sm[1]) + (sm[2] + sm[3]);
                 // |bf16(r)| <= |r| (1 + 2^-8): a bound on the sum of |lo|
-                lo_abs = cold ? lo_cap : ((la[0] + la[1]) + (la[2] + la[3])) * (1.0f + 1.0f / 256.0f);
+                lo_side = cold ? (sd == 0 ? cap0 : cap1) : ((la[0] + la[1]) + (la[2] + la[3])) * (1.0f + 1.0f / 256.0f);
             }
+            st_shared_f32(xch_addr(1, sd), ps_side);
+            st_shared_f32(xch_addr(2, sd), lo_side);
+            ok = pair_all(qw, ok);
+            const float ps = ld_shared_f32(xch_addr(1, 0)) + ld_shared_f32(xch_addr(1, 1));
+            const float lo_abs = ld_shared_f32(xch_addr(2, 0)) + ld_shared_f32(xch_addr(2, 1));
             lsum = lsum * alpha + ps;
             skipped *= alpha;
             // PV(g-1) must be done before O is rescaled; without a rescale this
             // warp does not wait for it.  Every tile has one PV, PV(j) commits to
             // O_DONE[j % 2], and S_FULL(g) (QK(g) retired, issued after PV(g-2))
             // means PV(g-3) has retired: the barrier is at most one phase behind
-            // the one waited for, so a parity wait cannot alias.
+            // the one waited for, so a parity wait cannot alias.  Side sd
+            // rescales O columns [128 sd, 128 sd + 128).
             const bool need_o = __any_sync(0xffffffffu, rescale);
-            if (need_o) {
-                if (!wait_bar_warp(c, bar_addr(c, BAR_O_DONE + ((g - 1) & 1u)), ((g - 1) >> 1) & 1u)) { ok = false; break; }
+            if (ok && need_o) {
+                if (!wait_bar_warp(c, bar_addr(c, BAR_O_DONE + ((g - 1) & 1u)), ((g - 1) >> 1) & 1u)) ok = false;
                 tc_fence_after();
-            }
-            if (need_o) {
-                const float f = rescale ? alpha : 1.f;
+                if (ok) {
+                    const float f = rescale ? alpha : 1.f;
 #pragma unroll 1
-                for (int cc = 0; cc < 8; ++cc) {
-                    uint32_t v[32];
-                    tmem_ld32(c.tmem + kTmemO + lane_base + 32 * cc, v);
-                    tmem_wait_ld();
+                    for (int cc = 0; cc < 4; ++cc) {
+                        const uint32_t oa = c.tmem + kTmemO + lane_base + 128 * sd + 32 * cc;
+                        uint32_t v[32];
+                        tmem_ld32(oa, v);
+                        tmem_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * f);
-                    tmem_st32(c.tmem + kTmemO + lane_base + 32 * cc, v);
+                        for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * f);
+                        tmem_st32(oa, v);
+                    }
                 }
             }
-            // vote on skipping the lo half: sum|lo| x max|V| (this CTA's dims) bounds what skipping drops
+            // vote on skipping the lo half: sum|lo| x max|V| (this CTA's dims)
+            // bounds what skipping drops; both sides reach the same vote
             {
                 const float cand = skipped + lo_abs * vmax;
                 const bool mine = (h >= H) || cold || (cand <= kLoBudget * lsum);
                 const bool warp_ok = __all_sync(0xffffffffu, mine);
-                if (warp_ok) skipped = cand;  // counted even if another warp vetoes: conservative
-                if (lane == 0) st_shared_u32(c.sb + kOffVote + (sbuf * 4 + warp) * 4, warp_ok ? 1u : 0u);
+                if (warp_ok) skipped = cand;  // counted even if another quarter vetoes: conservative
+                if (sd == 0 && lane == 0) st_shared_u32(c.sb + kOffVote + (sbuf * 4 + qw) * 4, warp_ok ? 1u : 0u);
             }
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_local(bar_addr(c, BAR_P_FULL + sbuf));
             o_init = true;
-            if (i + 1 < n && !take_peer(g + 1)) { ok = false; break; }
+            if (ok && i + 1 < n) ok = take_peer(g + 1);
         }
         if (ok && n > 0) {  // the unit's last PV (PV(g-1)); earlier ones retired before it
             if (!wait_bar_warp(c, bar_addr(c, BAR_O_DONE + ((g - 1) & 1u)), ((g - 1) >> 1) & 1u)) ok = false;
@@ -999,6 +1026,8 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, UnitDesc* units, in
             *c.abort = 1u;
             break;
         }
+        if (sd != 0) continue;  // side 0 finishes the unit and stages the next Q
+        tc_fence_after();       // side 1's rescales of O are complete (before the barrier)
         // ---- finish: final bf16 output, or an fp32 partial for the merge kernel ----
         if (d.s_r == 1) {
             const float M = fmaxf(m_used, sink2);
@@ -1055,7 +1084,7 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, UnitDesc* units, in
         // All TMEM reads of O are complete (tcgen05.wait::ld) before the next
         // unit's Q is staged; its first PV (which overwrites O) waits for Q.
         tc_fence_before();
-        softmax_bar();
+        side0_bar();
     }
     if (!ok) err |= SMLA_DEV_TIMEOUT;
 }
@@ -1361,7 +1390,7 @@ __global__ void __launch_bounds__(kThreads, 1) smla_decode_kernel(const KParams 
         }
         mbar_init(bar_addr(c, BAR_O_DONE), 1);
         mbar_init(bar_addr(c, BAR_O_DONE + 1), 1);
-        mbar_init(bar_addr(c, BAR_Q_READY), kSoftmaxWarps);
+        mbar_init(bar_addr(c, BAR_Q_READY), kSideWarps);
         mbar_init(bar_addr(c, BAR_MMA_FINAL), 1);
         fence_mbar_init_cluster();
     }
