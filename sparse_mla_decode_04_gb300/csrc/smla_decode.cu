@@ -928,6 +928,10 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, UnitDesc* units, in
             const float cap0 = mt0 == -INFINITY ? 0.f : capk * ex2_approx(mt0 - msub);
             const float cap1 = mt1 == -INFINITY ? 0.f : capk * ex2_approx(mt1 - msub);
             const bool cold = __all_sync(0xffffffffu, (h >= H) || (skipped * alpha + (cap0 + cap1) * vmax <= kLoBudget * lsum * alpha));
+            // The next tile's peer partial is taken now (this tile's scores are
+            // back in TMEM), so that QK's own-dims chain of the next tile runs
+            // while this tile's P is computed.
+            if (ok && i + 1 < n) ok = take_peer(g + 1);
             // ---- pass 2: P = 2^(s - m) as a bf16 pair hi = bf16(p), lo = bf16(p - hi),
             // written over this side's columns one 16-entry step at a time:
             // entries 16 q .. 16 q + 15 become hi in columns [16 q, 16 q + 8) and
@@ -1015,7 +1019,6 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, UnitDesc* units, in
             __syncwarp();
             if (lane == 0) mbar_arrive_local(bar_addr(c, BAR_P_FULL + sbuf));
             o_init = true;
-            if (ok && i + 1 < n) ok = take_peer(g + 1);
         }
         if (ok && n > 0) {  // the unit's last PV (PV(g-1)); earlier ones retired before it
             if (!wait_bar_warp(c, bar_addr(c, BAR_O_DONE + ((g - 1) & 1u)), ((g - 1) >> 1) & 1u)) ok = false;
