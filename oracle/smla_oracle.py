@@ -301,3 +301,114 @@ def plan_num_splits(num_rows: int, num_heads: int, kv_len: int, coeffs: dict, s_
         if best is None or c < best:
             best_s, best = s, c
     return best_s
+
+
+# ---------------------------------------------------------------------------
+# cache writer: latent rows -> FP8 + UE8M0 cache entries
+# ---------------------------------------------------------------------------
+# "[ROCm][DSV4][Perf] Optimize Triton sparse-MLA decode on gfx950", section
+# "Design", last paragraph: the cache writers store NoPE dims as FP8 with one
+# UE8M0 scale per 64 dims, cap the UE8M0 codes at 254 and canonicalise RoPE
+# NaNs.  Readings (stated in the design notes): the scale of a group is the
+# smallest power of two that brings the group's largest magnitude within the
+# e4m3 range (448); codes are clamped to [0, 254]; values are rounded to
+# nearest, ties to even, saturating at +-448; a NaN NoPE value is stored as
+# 0x7F, a value that rounds to zero as 0x00 (+0), and a NaN RoPE value as the
+# canonical bf16 NaN 0x7FC0.
+E4M3_MAX = 448.0
+BF16_CANONICAL_NAN = 0x7FC0
+
+# the 127 non-negative finite e4m3 codes 0x00..0x7E, ascending in value
+_E4M3_POS = E4M3_TABLE[:0x7F]
+
+
+def ue8m0_code_for(amax: float) -> int:
+    """Smallest code c in [0, 254] with amax <= 448 * 2**(c - 127); 254 when
+    none fits (an infinite amax)."""
+    if not amax > 0.0:  # zero (or an all-NaN group)
+        return 0
+    for c in range(0, 255):
+        if amax <= E4M3_MAX * math.ldexp(1.0, c - 127):
+            return c
+    return 254
+
+
+def e4m3_encode(q: float) -> int:
+    """Round to the nearest e4m3 value, ties to the even code, saturating at
+    +-448; NaN -> 0x7F; a result of zero -> 0x00."""
+    if math.isnan(q):
+        return 0x7F
+    mag = min(abs(q), E4M3_MAX)
+    i = int(np.searchsorted(_E4M3_POS, mag))  # first value >= mag
+    if i < len(_E4M3_POS) and _E4M3_POS[i] == mag:
+        code = i
+    else:
+        lo, hi = i - 1, i
+        dlo, dhi = mag - _E4M3_POS[lo], _E4M3_POS[hi] - mag
+        code = lo if (dlo < dhi or (dlo == dhi and lo % 2 == 0)) else hi
+    if code == 0:
+        return 0x00
+    return code | (0x80 if q < 0 else 0)
+
+
+def cache_write_row(bits) -> tuple:
+    """One latent row (uint16 bf16 bits [512]) -> (entry bytes [576], scale
+    bytes [8])."""
+    bits = np.asarray(bits, dtype=np.uint16)
+    x = bf16_bits_to_f64(bits)
+    entry = np.zeros(ENTRY_BYTES, dtype=np.uint8)
+    sc = np.zeros(8, dtype=np.uint8)
+    for g in range(N_SCALES):
+        grp = x[g * SCALE_GROUP:(g + 1) * SCALE_GROUP]
+        finite_or_inf = grp[~np.isnan(grp)]
+        amax = float(np.max(np.abs(finite_or_inf))) if finite_or_inf.size else 0.0
+        c = ue8m0_code_for(amax)
+        sc[g] = c
+        for d in range(SCALE_GROUP):
+            entry[g * SCALE_GROUP + d] = e4m3_encode(grp[d] * math.ldexp(1.0, 127 - c))
+    rope = bits[NOPE_DIMS:].copy()
+    nan = ((rope & 0x7F80) == 0x7F80) & ((rope & 0x007F) != 0)
+    rope[nan] = BF16_CANONICAL_NAN
+    entry[NOPE_DIMS:] = rope.astype("<u2").view(np.uint8)
+    return entry, sc
+
+
+def cache_write(latent_bits, slots, pool, scales):
+    """Write rows i with 0 <= slots[i] < len(pool) into pool / scales (numpy
+    arrays, modified in place); other slots are skipped.  Returns the number of
+    rows skipped for an out-of-range slot (slot -1 is a deliberate skip)."""
+    bad = 0
+    for i, s in enumerate(np.asarray(slots).tolist()):
+        if s == -1:
+            continue
+        if s < -1 or s >= pool.shape[0]:
+            bad += 1
+            continue
+        pool[s], scales[s] = cache_write_row(latent_bits[i])
+    return bad
+
+
+# ---------------------------------------------------------------------------
+# top-k selection: the producer of main_idx
+# ---------------------------------------------------------------------------
+# The step before the decode: each row's top-k index list (-1 = invalid slot)
+# is the k positions of [0, L_r) with the largest scores.  The pages name the
+# producer (the indexer top-k path and its cp-gather, "8k/1k TP8 follow-up",
+# item 2) but not how scores are made, so scores are an input here.
+# Readings: order by score descending, ties by position ascending; NaN scores
+# are never selected; rows with fewer than k selectable positions are padded
+# with -1.
+def topk_indices(scores, lens, k: int) -> np.ndarray:
+    scores = np.asarray(scores, dtype=np.float32)
+    R = scores.shape[0]
+    out = np.full((R, k), -1, dtype=np.int32)
+    for r in range(R):
+        L = int(lens[r])
+        s = scores[r, :L].astype(np.float64)
+        pos = np.arange(L)
+        keep = ~np.isnan(s)
+        s, pos = s[keep], pos[keep]
+        order = np.lexsort((pos, -s))  # last key first: score descending, then position
+        take = order[:k]
+        out[r, :take.size] = pos[take]
+    return out
