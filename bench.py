@@ -366,6 +366,69 @@ def per_config_lines(names, dev, flush_buf, stream, peaks, steps: int, warmup: i
     return res
 
 
+def next_rows_lines(dev, flush_buf, stream, peaks, steps: int, warmup: int = 3):
+    """The two producers beside the decode, each timed alone (CUDA events on
+    the launching stream, L2 flushed before each step), against the HBM
+    roofline of their algorithmic bytes:
+      cache_write: 4M latent rows (bf16 [4M, 512]) written to a random
+        permutation of 4M cache slots; 1024 B read + 584 B written + 8 B slot
+        per row;
+      topk_indices: the decode's largest shape, 64 rows x 1M scores, k = 2048;
+        4 B read per score + 4 B written per index."""
+    import gc
+    import torch
+    import sparse_mla_decode_04_gb300 as smla
+
+    res = {}
+
+    def timed(fn):
+        ms = []
+        for i in range(warmup + steps):
+            with torch.cuda.stream(stream):
+                flush_buf.fill_(i & 0xFF)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+            stream.synchronize()
+            if i >= warmup:
+                ms.append(e0.elapsed_time(e1))
+        return statistics.mean(ms) / 1e3
+
+    g = torch.Generator(device=dev)
+    g.manual_seed(77)
+    n = 4 << 20
+    lat = (torch.randn((n, 512), generator=g, device=dev)).to(torch.bfloat16)
+    slots = torch.randperm(n, generator=g, device=dev)
+    pool = torch.empty((n, 576), dtype=torch.uint8, device=dev)
+    sc = torch.empty((n, 8), dtype=torch.uint8, device=dev)
+    st = stream.cuda_stream
+    t = timed(lambda: smla.cache_write(lat, slots, pool, sc, stream=st))
+    nb = n * (1024 + 584 + 8)
+    res["cache_write"] = {"rows": n, "us_per_call": t * 1e6, "GB_per_s": nb / t / 1e9,
+                          "roofline": {"bound": "hbm", "achieved": nb / t / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                       "frac": nb / t / 1e9 / peaks["hbm_gbs"], "algorithmic_bytes": nb}}
+    log(f"next cache_write: {t * 1e6:.1f} us, {nb / t / 1e9:.0f} GB/s")
+    del lat, slots, pool, sc
+    gc.collect()
+    torch.cuda.empty_cache()
+    R, L, k = 64, 1 << 20, 2048
+    scores = torch.randn((R, L), generator=g, device=dev)
+    lens = torch.full((R,), L, dtype=torch.int32, device=dev)
+    out = torch.empty((R, k), dtype=torch.int32, device=dev)
+    t = timed(lambda: smla.topk_indices(scores, lens, k, out=out, stream=st))
+    nb = R * L * 4 + R * k * 4 + R * 4
+    res["topk_indices"] = {"rows": R, "positions": L, "k": k, "us_per_call": t * 1e6, "GB_per_s": nb / t / 1e9,
+                           "roofline": {"bound": "hbm", "achieved": nb / t / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                        "frac": nb / t / 1e9 / peaks["hbm_gbs"], "algorithmic_bytes": nb}}
+    log(f"next topk_indices: {t * 1e6:.1f} us, {nb / t / 1e9:.0f} GB/s")
+    del scores, lens, out
+    gc.collect()
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_gpu(args):
     import gc
     import torch
@@ -493,6 +556,7 @@ def run_gpu(args):
     if rank == 0 and world == 1 and not args.no_per_config:
         names = [n for n in PER_CONFIG if n != args.workload]
         line["per_config"] = per_config_lines(names, dev, flush_buf, stream, peaks, args.config_steps, 3)
+        line["next_rows"] = next_rows_lines(dev, flush_buf, stream, peaks, args.config_steps)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

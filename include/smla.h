@@ -189,6 +189,51 @@ smla_status smla_read_device_error(void* workspace, uint32_t* flags, smla_stream
 /* Static, NUL-terminated description of a status code. */
 const char* smla_status_string(smla_status status);
 
+/*
+ * Cache writer: quantises latent rows into the cache layout smla_decode reads.
+ * Source: "[ROCm][DSV4][Perf] Optimize Triton sparse-MLA decode on gfx950"
+ * (vLLM pull request 52212), section "Design", last paragraph: the cache
+ * writers store FP8 NoPE with UE8M0 scales, cap the codes at 254 and
+ * canonicalise RoPE NaNs.  For each row i with slots[i] >= 0:
+ *   - NoPE group g (dims 64g .. 64g+63, g < 7): code_g = the smallest c in
+ *     [0, 254] with max|x| <= 448 * 2^(c-127) (254 when none fits);
+ *     pool[s][d] = e4m3(x[d] * 2^(127-code_g)), round to nearest even,
+ *     saturating at +-448; a NaN value -> 0x7F; a value rounding to zero -> 0x00;
+ *     scales[s][g] = code_g, scales[s][7] = 0;
+ *   - RoPE: pool[s][448 + 2i .. ] = x[448 + i] (bf16, little-endian), a NaN
+ *     becoming 0x7FC0.
+ * Arguments (DEVICE pointers, caller-owned): latent bf16 [num_rows][512]
+ * (16-byte aligned); slots int64 [num_rows] (8-byte aligned), -1 = skip the
+ * row; pool u8 [n_pool][576] (16-byte aligned) and scales u8 [n_pool][8]
+ * (8-byte aligned), written in place; dev_error: optional uint32 word (NULL
+ * or 4-byte aligned) that gets SMLA_DEV_BAD_INDEX for a slot < -1 or >= n_pool
+ * (that row is skipped).  Two rows with the same slot race.  Host checks as
+ * for smla_decode; num_rows = 0 launches nothing.  One kernel launch on
+ * `stream`; allocates nothing.
+ */
+smla_status smla_cache_write(const void* latent, int64_t num_rows, const int64_t* slots, void* pool,
+                             void* scales, int64_t n_pool, uint32_t* dev_error, smla_stream_t stream);
+
+/* Largest k accepted by smla_topk_indices. */
+#define SMLA_TOPK_MAX_K 4096
+
+/*
+ * Top-k producer: the decode's top-k index list from per-position scores.
+ * The pages name this step (the indexer top-k path whose cp-gather the vLLM
+ * page's comment "8k/1k TP8 follow-up", item 2, reworks) but not how its
+ * scores are made, so the scores are an input.  For each row r:
+ * out[r][0 .. k-1] = the positions p in [0, min(lens[r], stride)) with the
+ * largest scores[r][p], ordered by score descending and then by position
+ * ascending (-0 equals +0); positions with a NaN score are never taken; slots
+ * left over when fewer than k positions are selectable hold -1.
+ * Arguments (DEVICE pointers, caller-owned, 4-byte aligned): scores float32
+ * [num_rows][stride]; lens int32 [num_rows]; out int32 [num_rows][k].
+ * 1 <= k <= SMLA_TOPK_MAX_K, 0 <= stride < 2^31.  One kernel launch on
+ * `stream` (one CTA per row); allocates nothing.
+ */
+smla_status smla_topk_indices(const float* scores, int64_t stride, const int32_t* lens, int32_t num_rows,
+                              int32_t k, int32_t* out, smla_stream_t stream);
+
 /* Bytes of the scratch array built into the library for smla_decode_static_scratch
  * (48 MiB).  It holds the workspace layout of smla_workspace_bytes: with
  * U = max(num_rows * num_splits, num_rows + 95) partial units of

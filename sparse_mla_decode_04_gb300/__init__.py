@@ -18,7 +18,8 @@ from .smla import (  # noqa: F401
     SMLA_DEV_TIMEOUT, SMLA_ERR_BAD_SHAPE, SMLA_ERR_CUDA, SMLA_ERR_MISALIGNED, SMLA_ERR_NULL_POINTER,
     SMLA_ERR_UNSUPPORTED_DEVICE, SMLA_ERR_WORKSPACE_TOO_SMALL, SMLA_OK, SmlaError, load_library, make_args,
     smla_decode, smla_decode_args, smla_plan_default_coeffs, smla_plan_num_splits, smla_plan_num_splits_ex,
-    smla_read_device_error, smla_status_string, smla_workspace_bytes,
+    smla_read_device_error, smla_status_string, smla_workspace_bytes, smla_cache_write, smla_topk_indices,
+    cache_write, topk_indices,
 )
 
 

@@ -1,6 +1,6 @@
 """Builds libsmla.so in-tree with nvcc for sm_103a.
 
-Two translation units (kernel + host C ABI) are compiled in parallel and
+The translation units (kernels + host C ABI) are compiled in parallel and
 linked against the static CUDA runtime.  Host code is compiled with
 -ffp-contract=off so that the planner's floating-point cost model evaluates
 identically on x86-64 and aarch64.
@@ -22,7 +22,7 @@ LIB_DIR = PKG / "lib"
 LIB_NAME = "libsmla.so"
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
-SOURCES = ["smla_decode.cu", "smla_host.cpp", "smla_static_scratch.cu"]
+SOURCES = ["smla_decode.cu", "smla_host.cpp", "smla_static_scratch.cu", "smla_cache_write.cu", "smla_topk.cu"]
 
 
 def nvcc_path() -> str:

@@ -1,0 +1,152 @@
+// Cache writer: latent rows (bf16, 448 NoPE + 64 RoPE dims) -> the decode's
+// cache layout (448 e4m3 bytes + 64 bf16, one UE8M0 code per 64 NoPE dims).
+//
+// Method ("[ROCm][DSV4][Perf] Optimize Triton sparse-MLA decode on gfx950",
+// section "Design", last paragraph): the writers cap UE8M0 codes at 254 and
+// canonicalise RoPE NaNs.  Per 64-dim group the code is the smallest power of
+// two that brings the group's largest magnitude within the e4m3 range (448),
+// clamped to [0, 254]; each value is stored as e4m3(x * 2^(127 - code)),
+// rounded to nearest, ties to even, saturating at +-448.  A NaN NoPE value is
+// stored as 0x7F, a value that rounds to zero as 0x00, a NaN RoPE value as
+// the canonical bf16 NaN 0x7FC0; every other RoPE value is copied unchanged.
+//
+// One warp per row: lane l < 28 converts NoPE dims [16 l, 16 l + 16) (group
+// l / 4, its amax reduced over 4 lanes), lanes 28..31 copy 16 RoPE dims each.
+// The path is HBM-bound: 1024 bytes read and 584 written per row.
+#include <algorithm>
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_fp8.h>
+
+#include "smla.h"
+#include "smla_internal.h"
+
+namespace smla {
+namespace {
+
+constexpr int kWarpsPerBlock = 8;
+
+// Smallest code c in [0, 254] with amax <= 448 * 2^(c - 127), from the fp32
+// bits of amax (>= 0, not NaN): amax = m 2^e, 448 = 1.75 2^8, so
+// c = 127 + e - 8 + [m > 1.75], clamped; +inf gives the cap.
+__device__ __forceinline__ uint32_t ue8m0_code(float amax) {
+    const uint32_t b = __float_as_uint(amax);
+    const int be = (int)(b >> 23);  // biased exponent
+    if (be == 255) return 254u;
+    if (be == 0) return 0u;  // zero or subnormal: 448 x 2^-127 already covers it
+    const int c = be - 8 + ((b & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+    return (uint32_t)min(max(c, 0), 254);
+}
+
+// 2^(127 - code) as fp32 (code 254 gives the subnormal 2^-127).
+__device__ __forceinline__ float inv_scale(uint32_t code) {
+    return code <= 253u ? __uint_as_float((254u - code) << 23) : __uint_as_float(0x00400000u);
+}
+
+// Two values -> two e4m3 bytes (low byte = a).
+__device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
+    uint32_t r = (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+    uint32_t lo = r & 0xFFu, hi = r >> 8;
+    if (a != a) lo = 0x7Fu;
+    else if ((lo & 0x7Fu) == 0u) lo = 0u;
+    if (b != b) hi = 0x7Fu;
+    else if ((hi & 0x7Fu) == 0u) hi = 0u;
+    return lo | (hi << 8);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint32_t canon_nan_bf16x2(uint32_t w) {
+    uint32_t lo = w & 0xFFFFu, hi = w >> 16;
+    if ((lo & 0x7FFFu) > 0x7F80u) lo = 0x7FC0u;
+    if ((hi & 0x7FFFu) > 0x7F80u) hi = 0x7FC0u;
+    return lo | (hi << 16);
+}
+
+__global__ void __launch_bounds__(32 * kWarpsPerBlock) smla_cache_write_kernel(
+    const uint4* __restrict__ latent, int64_t num_rows, const int64_t* __restrict__ slots, uint8_t* __restrict__ pool,
+    uint8_t* __restrict__ scales, int64_t n_pool, uint32_t* err) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warp0 = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+    const int64_t nwarps = (int64_t)gridDim.x * kWarpsPerBlock;
+    uint32_t bad = 0;
+    for (int64_t row = warp0; row < num_rows; row += nwarps) {
+        const int64_t s = __ldg(slots + row);
+        if (s == -1) continue;
+        if (s < -1 || s >= n_pool) {
+            bad = 1;
+            continue;
+        }
+        const uint4 v0 = __ldg(latent + row * 64 + 2 * lane);      // dims 16 l .. 16 l + 7
+        const uint4 v1 = __ldg(latent + row * 64 + 2 * lane + 1);  // dims 16 l + 8 .. 16 l + 15
+        const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+        uint8_t* dst = pool + s * SMLA_ENTRY_BYTES;
+        // every lane takes part in the group reductions (shuffles); RoPE lanes
+        // contribute a dummy zero that never leaves their own 4-lane group
+        float amax = 0.f;
+        if (lane < 28) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
+        }
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        const uint32_t code = ue8m0_code(amax);
+        if (lane < 28) {
+            const float f = inv_scale(code);
+            uint32_t o[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t p0 = e4m3x2(bf16_lo(w[2 * i]) * f, bf16_hi(w[2 * i]) * f);
+                const uint32_t p1 = e4m3x2(bf16_lo(w[2 * i + 1]) * f, bf16_hi(w[2 * i + 1]) * f);
+                o[i] = p0 | (p1 << 16);
+            }
+            *reinterpret_cast<uint4*>(dst + 16 * lane) = make_uint4(o[0], o[1], o[2], o[3]);
+        } else {
+            uint4 r0, r1;
+            r0.x = canon_nan_bf16x2(w[0]); r0.y = canon_nan_bf16x2(w[1]);
+            r0.z = canon_nan_bf16x2(w[2]); r0.w = canon_nan_bf16x2(w[3]);
+            r1.x = canon_nan_bf16x2(w[4]); r1.y = canon_nan_bf16x2(w[5]);
+            r1.z = canon_nan_bf16x2(w[6]); r1.w = canon_nan_bf16x2(w[7]);
+            uint4* rd = reinterpret_cast<uint4*>(dst + SMLA_NOPE_DIMS + 32 * (lane - 28));
+            rd[0] = r0;
+            rd[1] = r1;
+        }
+        // the 7 codes (lanes 0, 4, ..., 24) and a zero pad byte, one 8-byte store
+        uint32_t lo = 0, hi = 0;
+#pragma unroll
+        for (int g = 0; g < 7; ++g) {
+            const uint32_t cg = __shfl_sync(0xffffffffu, code, 4 * g);
+            if (g < 4) lo |= cg << (8 * g); else hi |= cg << (8 * (g - 4));
+        }
+        if (lane == 0) *reinterpret_cast<uint2*>(scales + s * SMLA_SCALE_BYTES) = make_uint2(lo, hi);
+    }
+    if (err != nullptr && __any_sync(0xffffffffu, bad != 0) && lane == 0) atomicOr(err, SMLA_DEV_BAD_INDEX);
+}
+
+bool aligned_to(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+}  // namespace smla
+
+extern "C" smla_status smla_cache_write(const void* latent, int64_t num_rows, const int64_t* slots, void* pool,
+                                        void* scales, int64_t n_pool, uint32_t* dev_error, smla_stream_t stream) {
+    using namespace smla;
+    if (num_rows < 0 || n_pool < 0) return SMLA_ERR_BAD_SHAPE;
+    if (num_rows == 0) return SMLA_OK;
+    if (latent == nullptr || slots == nullptr || pool == nullptr || scales == nullptr) return SMLA_ERR_NULL_POINTER;
+    if (!aligned_to(latent, 16) || !aligned_to(pool, 16) || !aligned_to(slots, 8) || !aligned_to(scales, 8) ||
+        !aligned_to(dev_error, 4))
+        return SMLA_ERR_MISALIGNED;
+    const smla_status dev = check_device_only();
+    if (dev != SMLA_OK) return dev;
+    int sms = 0, d = 0;
+    if (cudaGetDevice(&d) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, d) != cudaSuccess)
+        return SMLA_ERR_CUDA;
+    const int64_t blocks_needed = (num_rows + kWarpsPerBlock - 1) / kWarpsPerBlock;
+    const int blocks = (int)std::min<int64_t>(blocks_needed, (int64_t)sms * 8);
+    smla_cache_write_kernel<<<blocks, 32 * kWarpsPerBlock, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint4*>(latent), num_rows, slots, static_cast<uint8_t*>(pool), static_cast<uint8_t*>(scales),
+        n_pool, dev_error);
+    return cudaGetLastError() == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA;
+}

@@ -70,6 +70,8 @@ smla_status check_decode_args(const smla_decode_args* a) {
     return SMLA_OK;
 }
 
+smla_status check_device_only() { return check_device(); }
+
 smla_status check_decode_call(const smla_decode_args* a, const void* workspace, size_t ws_bytes) {
     if (a == nullptr || workspace == nullptr) return SMLA_ERR_NULL_POINTER;
     const smla_status st = check_decode_args(a);

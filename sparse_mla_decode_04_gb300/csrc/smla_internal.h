@@ -46,6 +46,8 @@ inline WorkspaceLayout workspace_layout(int rows, int heads, int splits) {
 // would return, and touch nothing on the device.
 smla_status check_decode_args(const smla_decode_args* a);
 smla_status check_decode_call(const smla_decode_args* a, const void* workspace, size_t ws_bytes);
+// The device check alone (compute capability 10.3, cached per device).
+smla_status check_device_only();
 
 // Host-validated launch of the decode and merge kernels (defined in smla_decode.cu).
 smla_status launch_decode(const smla_decode_args* args, void* workspace, cudaStream_t stream);

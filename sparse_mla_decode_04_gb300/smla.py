@@ -172,3 +172,49 @@ def smla_decode_static_scratch(args: smla_decode_args, stream: int = 0) -> int:
     fn.argtypes = [POINTER(smla_decode_args), c_void_p]
     fn.restype = c_int
     return fn(ctypes.byref(args), c_void_p(stream))
+
+
+def smla_cache_write(latent: int, num_rows: int, slots: int, pool: int, scales: int, n_pool: int,
+                     dev_error: Optional[int] = None, stream: int = 0) -> int:
+    """Quantise latent rows into the cache (raw device addresses).  Returns the status."""
+    fn = load_library().smla_cache_write
+    fn.argtypes = [c_void_p, c_int64, c_void_p, c_void_p, c_void_p, c_int64, c_void_p, c_void_p]
+    fn.restype = c_int
+    return fn(c_void_p(latent), num_rows, c_void_p(slots), c_void_p(pool), c_void_p(scales), n_pool,
+              c_void_p(dev_error) if dev_error else None, c_void_p(stream))
+
+
+def smla_topk_indices(scores: int, stride: int, lens: int, num_rows: int, k: int, out: int, stream: int = 0) -> int:
+    """Per-row top-k positions of a score matrix (raw device addresses).  Returns the status."""
+    fn = load_library().smla_topk_indices
+    fn.argtypes = [c_void_p, c_int64, c_void_p, c_int32, c_int32, c_void_p, c_void_p]
+    fn.restype = c_int
+    return fn(c_void_p(scores), stride, c_void_p(lens), num_rows, k, c_void_p(out), c_void_p(stream))
+
+
+def cache_write(latent, slots, pool, scales, dev_error=None, stream: Optional[int] = None) -> None:
+    """smla_cache_write on torch device tensors: latent bf16 [n, 512], slots int64
+    [n], pool uint8 [N, 576], scales uint8 [N, 8] (written in place)."""
+    import torch
+
+    s = torch.cuda.current_stream().cuda_stream if stream is None else stream
+    st = smla_cache_write(latent.data_ptr(), int(latent.shape[0]), slots.data_ptr(), pool.data_ptr(),
+                          scales.data_ptr(), int(pool.shape[0]),
+                          dev_error.data_ptr() if dev_error is not None else None, s)
+    if st != SMLA_OK:
+        raise SmlaError(st, "smla_cache_write")
+
+
+def topk_indices(scores, lens, k: int, out=None, stream: Optional[int] = None):
+    """smla_topk_indices on torch device tensors: scores float32 [R, stride],
+    lens int32 [R].  Returns int32 [R, k]."""
+    import torch
+
+    R = int(scores.shape[0])
+    if out is None:
+        out = torch.empty((R, k), dtype=torch.int32, device=scores.device)
+    s = torch.cuda.current_stream().cuda_stream if stream is None else stream
+    st = smla_topk_indices(scores.data_ptr(), int(scores.stride(0)), lens.data_ptr(), R, k, out.data_ptr(), s)
+    if st != SMLA_OK:
+        raise SmlaError(st, "smla_topk_indices")
+    return out
