@@ -43,6 +43,7 @@ __global__ void __launch_bounds__(kThreadsTopk) smla_topk_kernel(const float* __
     const int r = blockIdx.x, tid = threadIdx.x;
     const float* row = scores + (int64_t)r * stride;
     const int L = (int)min((int64_t)max(0, __ldg(lens + r)), stride);  // lengths past the row's capacity are cut
+    const bool vec4 = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;    // 16-byte loads where the row allows
     // ---- radix select: the k-th largest key among keys >= 1
     if (tid == 0) { s_prefix = 0u; s_mask = 0u; s_need = (uint32_t)k; }
     const int shifts[3] = {21, 10, 0};
@@ -54,9 +55,19 @@ __global__ void __launch_bounds__(kThreadsTopk) smla_topk_kernel(const float* __
         for (int i = tid; i < nb; i += kThreadsTopk) hist[i] = 0u;
         __syncthreads();
         const uint32_t prefix = s_prefix, mask = s_mask;
-        for (int i = tid; i < L; i += kThreadsTopk) {
-            const uint32_t key = sort_key(__ldg(row + i));
+        auto count = [&](float f) {
+            const uint32_t key = sort_key(f);
             if (key != 0u && (key & mask) == prefix) atomicAdd(&hist[(key >> sh) & (uint32_t)(nb - 1)], 1u);
+        };
+        if (vec4) {
+            const float4* row4 = reinterpret_cast<const float4*>(row);
+            for (int i = tid; i < L / 4; i += kThreadsTopk) {
+                const float4 v = __ldg(row4 + i);
+                count(v.x); count(v.y); count(v.z); count(v.w);
+            }
+            for (int i = (L & ~3) + tid; i < L; i += kThreadsTopk) count(__ldg(row + i));
+        } else {
+            for (int i = tid; i < L; i += kThreadsTopk) count(__ldg(row + i));
         }
         __syncthreads();
         if (tid == 0) {  // walk the bins from the top until the k-th key's bin
@@ -96,24 +107,23 @@ __global__ void __launch_bounds__(kThreadsTopk) smla_topk_kernel(const float* __
             const uint32_t slot = atomicAdd(&s_count, 1u);
             sel[slot] = item;
         }
-        if (!take_all) {  // equal keys: block-wide exclusive count in position order
+        if (!take_all) {  // equal keys: taken in position order until need_eq
             const bool eq = key == T && key != 0u;
-            const uint32_t ballot = __ballot_sync(0xffffffffu, eq);
-            if ((tid & 31) == 0) s_warp[tid >> 5] = __popc(ballot);
-            __syncthreads();
-            uint32_t before = eq_base, chunk_total = 0;
-            for (int w = 0; w < kThreadsTopk / 32; ++w) {
-                const uint32_t c = s_warp[w];
-                if (w < (tid >> 5)) before += c;
-                chunk_total += c;
-            }
-            before += __popc(ballot & ((1u << (tid & 31)) - 1u));
-            if (eq && before < need_eq) {
-                const uint32_t slot = atomicAdd(&s_count, 1u);
-                sel[slot] = item;
+            const uint32_t chunk_total = (uint32_t)__syncthreads_count(eq);
+            if (chunk_total != 0u && eq_base < need_eq) {  // block-uniform: the rare chunks holding T
+                const uint32_t ballot = __ballot_sync(0xffffffffu, eq);
+                if ((tid & 31) == 0) s_warp[tid >> 5] = __popc(ballot);
+                __syncthreads();
+                uint32_t before = eq_base;
+                for (int w = 0; w < (tid >> 5); ++w) before += s_warp[w];
+                before += __popc(ballot & ((1u << (tid & 31)) - 1u));
+                if (eq && before < need_eq) {
+                    const uint32_t slot = atomicAdd(&s_count, 1u);
+                    sel[slot] = item;
+                }
+                __syncthreads();
             }
             eq_base += chunk_total;
-            __syncthreads();
         }
     }
     __syncthreads();
