@@ -186,6 +186,19 @@ smla_status smla_decode(const smla_decode_args* args, void* workspace, size_t ws
  */
 smla_status smla_read_device_error(void* workspace, uint32_t* flags, smla_stream_t stream);
 
+/*
+ * Diagnostic: sets the limit of every wait inside the decode kernel (each
+ * pipeline stage waits for the previous one with a bounded wait) for the
+ * launches that follow, in nanoseconds; 0 restores the default of 2 s.
+ * Returns the previous limit.  When a wait runs out, the kernel stops all its
+ * roles, lets the work it already issued finish, sets SMLA_DEV_TIMEOUT in the
+ * workspace error word and returns; the outputs of that call are undefined,
+ * and the next call (with a working limit) is unaffected.  Process-wide;
+ * thread-safe.  Meant for tests of that path: with the default limit a wait
+ * runs out only if the GPU stops making progress.
+ */
+uint64_t smla_set_wait_limit_ns(uint64_t ns);
+
 /* Static, NUL-terminated description of a status code. */
 const char* smla_status_string(smla_status status);
 

@@ -98,7 +98,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;        // O half: columns [0, 256)
 constexpr uint32_t kTmemS = 256;      // score / P buffers: [256, 320), [320, 384)
 constexpr uint32_t kTmemQ = 384;      // Q's peer dims, bf16 packed: [384, 512)
-constexpr uint64_t kWaitNs = 2000000000ull;  // bounded-wait limit (2 s)
+constexpr uint64_t kDrainNs = 2000000000ull;  // limit of the teardown waits for work already issued (2 s)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 // log2 units: P may grow to 2^32 before O is rescaled.  O then stays below
@@ -164,6 +164,7 @@ struct KParams {
     float* po;           // [units][2][H][256] unnormalised fp32 O, by dims half
     int units;           // num_rows * num_splits: the chunked plan's unit budget
     int unit_cap;        // partial slots in the workspace (>= units and >= rows + kMaxPairs - 1)
+    uint64_t wait_ns;    // limit of every pipeline wait (smla_set_wait_limit_ns; default 2 s)
 };
 
 struct UnitDesc {
@@ -325,6 +326,7 @@ struct Ctx {
     uint32_t tmem;            // TMEM base address
     uint32_t half;            // 0 or 1: output dims [256 half, 256 half + 256)
     volatile uint32_t* abort; // set by any role whose bounded wait gave up
+    uint64_t wait_ns;         // limit of a pipeline wait
 };
 
 __device__ __forceinline__ uint32_t bar_addr(const Ctx& c, uint32_t i) { return c.sb + kOffBar + 8 * i; }
@@ -337,7 +339,7 @@ __device__ __forceinline__ bool wait_bar(const Ctx& c, uint32_t bar, uint32_t pa
         for (int i = 0; i < 4; ++i)
             if (mbar_try_wait(bar, parity)) return true;
         if (*c.abort) return false;
-        if (global_timer_ns() - t0 > kWaitNs) {
+        if (global_timer_ns() - t0 > c.wait_ns) {
             *c.abort = 1u;
             return false;
         }
@@ -408,6 +410,18 @@ __device__ void producer_role(const KParams& p, const Ctx& c, const UnitDesc* un
     const smla_decode_args& a = p.a;
     const int lane = threadIdx.x & 31;
     uint32_t q = 0;
+    int64_t last_fill = -1;  // the last raw tile this warp filled (all of them go to its stage pw)
+    // Nothing this warp started may still be writing shared memory when it
+    // leaves, whether it finished or gave up: its cp.async copies are waited
+    // for, and so is the phase of its last fill, which completes once the
+    // bytes of that fill (bulk or cp.async) have landed.  Only this warp fills
+    // its stage, so the barrier cannot have moved past that phase.
+    auto drain = [&]() {
+        cp_async_wait_all();
+        if (last_fill >= 0)
+            mbar_wait_bounded(bar_addr(c, BAR_RAW_FULL + (uint32_t)pw), (uint32_t)((last_fill / kNR) & 1), kDrainNs);
+        __syncwarp();
+    };
     for (int ui = 0; ui < n_units; ++ui) {
         const UnitDesc d = units[ui];
         const int r = d.row;
@@ -474,7 +488,7 @@ __device__ void producer_role(const KParams& p, const Ctx& c, const UnitDesc* un
             } else if (ep != nullptr) {
                 bulk_prefetch_l2(ep, SMLA_ENTRY_BYTES);
             }
-            if (!wait_bar_warp(c, bar_addr(c, BAR_RAW_EMPTY + rs), rph ^ 1u)) return;
+            if (!wait_bar_warp(c, bar_addr(c, BAR_RAW_EMPTY + rs), rph ^ 1u)) { drain(); return; }
             const uint32_t full = bar_addr(c, BAR_RAW_FULL + rs);
             const uint32_t dst = c.sb + kOffRaw + rs * kRawStageBytes;
             if (run) {
@@ -504,8 +518,10 @@ __device__ void producer_role(const KParams& p, const Ctx& c, const UnitDesc* un
                 st_shared_u32(c.sb + kOffRawMask + rs * 4, mask);
                 mbar_arrive_local(full);  // the 33rd arrival, ordered after the mask store
             }
+            last_fill = (int64_t)q;
         }
     }
+    drain();
 }
 
 // ---------------------------------------------------------------------------
@@ -732,7 +748,7 @@ __device__ void mma_role(const Ctx& c, const UnitDesc* units, int n_units) {
     }
     // retire every MMA before TMEM is released
     mma_commit(bar_addr(c, BAR_MMA_FINAL));
-    mbar_wait_bounded<false>(bar_addr(c, BAR_MMA_FINAL), 0, kWaitNs);
+    mbar_wait_bounded(bar_addr(c, BAR_MMA_FINAL), 0, kDrainNs);
 }
 
 // ---------------------------------------------------------------------------
@@ -1361,6 +1377,7 @@ __global__ void __launch_bounds__(kThreads, 1) smla_decode_kernel(const KParams 
     Ctx c;
     c.sb = smem_addr(smem);
     c.half = blockIdx.x & 1u;
+    c.wait_ns = p.wait_ns;
     volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + kOffMisc);
     c.abort = misc + 1;
     int* s_tiles = reinterpret_cast<int*>(smem + kOffRaw);  // prologue only
@@ -1395,7 +1412,10 @@ __global__ void __launch_bounds__(kThreads, 1) smla_decode_kernel(const KParams 
         mbar_init(bar_addr(c, BAR_O_DONE + 1), 1);
         mbar_init(bar_addr(c, BAR_Q_READY), kSideWarps);
         mbar_init(bar_addr(c, BAR_MMA_FINAL), 1);
-        fence_mbar_init_cluster();
+        // the tensor core's commits and the bulk copies arrive on these
+        // barriers through the async proxy: their initialisation is released
+        // to it before first use
+        fence_mbar_init();
     }
     if (warp == kMmaWarp) {
         tmem_alloc(c.sb + kOffMisc, kTmemCols);
@@ -1549,6 +1569,7 @@ smla_status launch_decode(const smla_decode_args* args, void* workspace, cudaStr
     kp.po = reinterpret_cast<float*>(ws + L.off_po);
     kp.units = args->num_rows * args->num_splits;
     kp.unit_cap = unit_capacity(args->num_rows, args->num_splits);
+    kp.wait_ns = wait_limit_ns();
     // Persistent grid: CTA pairs (one CTA per output half) up to what is
     // co-resident (the stream plan can use every one of them), and enough
     // pairs that the chunked plan hands none more than kMaxUnitsPerPair units.

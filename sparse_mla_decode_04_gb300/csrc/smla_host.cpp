@@ -23,6 +23,9 @@ constexpr smla_plan_coeffs kGB300Coeffs = {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;
+std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
+
 // Device check, cached per device (thread-safe).
 std::atomic<int> g_dev_ok[64];  // 0 unknown, 1 sm_103, 2 other
 
@@ -71,6 +74,8 @@ smla_status check_decode_args(const smla_decode_args* a) {
 }
 
 smla_status check_device_only() { return check_device(); }
+
+uint64_t wait_limit_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
 
 smla_status check_decode_call(const smla_decode_args* a, const void* workspace, size_t ws_bytes) {
     if (a == nullptr || workspace == nullptr) return SMLA_ERR_NULL_POINTER;
@@ -143,6 +148,10 @@ smla_status smla_read_device_error(void* workspace, uint32_t* flags, smla_stream
     if (cudaStreamSynchronize(s) != cudaSuccess) return SMLA_ERR_CUDA;
     *flags = host;
     return SMLA_OK;
+}
+
+uint64_t smla_set_wait_limit_ns(uint64_t ns) {
+    return g_wait_ns.exchange(ns == 0 ? kDefaultWaitNs : ns, std::memory_order_relaxed);
 }
 
 const char* smla_status_string(smla_status status) {

@@ -49,6 +49,10 @@ smla_status check_decode_call(const smla_decode_args* a, const void* workspace, 
 // The device check alone (compute capability 10.3, cached per device).
 smla_status check_device_only();
 
+// Limit of every pipeline wait inside the decode kernel, in ns (set by
+// smla_set_wait_limit_ns; 2 s by default).
+uint64_t wait_limit_ns();
+
 // Host-validated launch of the decode and merge kernels (defined in smla_decode.cu).
 smla_status launch_decode(const smla_decode_args* args, void* workspace, cudaStream_t stream);
 

@@ -218,3 +218,12 @@ def topk_indices(scores, lens, k: int, out=None, stream: Optional[int] = None):
     if st != SMLA_OK:
         raise SmlaError(st, "smla_topk_indices")
     return out
+
+
+def smla_set_wait_limit_ns(ns: int) -> int:
+    """Set the decode kernel's wait limit for later launches (0 = default 2 s);
+    returns the previous limit (a diagnostic for tests of the timeout path)."""
+    fn = load_library().smla_set_wait_limit_ns
+    fn.argtypes = [ctypes.c_uint64]
+    fn.restype = ctypes.c_uint64
+    return int(fn(ns))

@@ -352,3 +352,26 @@ def test_nan_byte_in_a_selected_entry_propagates(cuda_device, dim):
     assert np.array_equal(np.isnan(l), np.isnan(rl))
     fin = ~np.isnan(ro)
     assert (np.abs(o[fin] - ro[fin]) <= 1e-2 + 1e-2 * np.abs(ro[fin])).all()
+
+
+def test_wait_limit_runs_out_and_the_next_call_is_clean(cuda_device):
+    """With a wait limit far below what the pipeline needs, the call still
+    returns, the workspace error word reports SMLA_DEV_TIMEOUT, and the next
+    call with the default limit matches the oracle: the kernel's give-up path
+    (every role leaves its loop, issued copies and MMAs are waited for, TMEM is
+    freed) leaves nothing behind."""
+    from sparse_mla_decode_04_gb300 import smla as S
+
+    p = small(H=128, seq_lens=(20000, 9000, 3000), topk=1024, swa=128, seed=41)
+    ws = smla.Workspace(p.num_rows, p.num_heads, 4)
+    prev = S.smla_set_wait_limit_ns(100)  # 100 ns: far below one tile
+    try:
+        for _ in range(3):
+            run_gpu(p, num_splits=4, workspace=ws)
+        flags = ws.read_error()
+    finally:
+        S.smla_set_wait_limit_ns(0)
+    assert prev == 2_000_000_000
+    assert flags & smla.SMLA_DEV_TIMEOUT
+    check(p, num_splits=4, workspace=ws, what="after timeouts")
+    assert ws.read_error() == 0
