@@ -120,10 +120,11 @@ constexpr uint32_t kOffXO = kOffQ + 65536;                         // own dims: 
 constexpr uint32_t kOffXP = kOffXO + kNXO * kHalfBytes;            // peer dims: [4 atoms][64][128 B]
 constexpr uint32_t kOffRaw = kOffXP + kHalfBytes;                  // [kNR][32][576 B]
 constexpr uint32_t kOffRawSc = kOffRaw + kNR * kRawStageBytes;     // [kNR][32] u64 scale codes
-constexpr uint32_t kOffRawMask = kOffRawSc + kNR * kRawBK * 8;     // [kNR] u32 valid masks
-constexpr uint32_t kOffXMask = kOffRawMask + 16;                   // [kNXO][2] u32 valid masks (64 entries)
-constexpr uint32_t kOffXVmax = kOffXMask + kNXO * 8;               // [kNXO][8 dequant warps] f32 max |V| bound
-constexpr uint32_t kOffVote = kOffXVmax + kNXO * 32;               // [2][4 head quarters] u32 lo-skip votes
+constexpr uint32_t kOffRawMask = kOffRawSc + kNR * kRawBK * 8;     // [kNR][4] u32: loaded, valid for A, for B
+constexpr uint32_t kOffXMask = kOffRawMask + kNR * 16;             // [kNXO][2 raw tiles][A, B] u32 valid masks
+constexpr uint32_t kOffXVmax = kOffXMask + kNXO * 16;              // [kNXO][8 dequant warps] f32 max |V| bound
+constexpr uint32_t kOffXPoison = kOffXVmax + kNXO * 32;            // [kNXO][8 dequant warps] u32 rows poisoned (bit 0 A, 1 B)
+constexpr uint32_t kOffVote = kOffXPoison + kNXO * 32;             // [2][4 head quarters] u32 lo-skip votes
 constexpr uint32_t kOffXch = kOffVote + 32;                        // [3][2 sides][128 heads] f32 side exchange
 constexpr uint32_t kOffBar = kOffXch + 3 * 2 * 128 * 4;         // mbarriers
 constexpr uint32_t kNumBars = 32;
@@ -165,6 +166,9 @@ struct KParams {
     int units;           // num_rows * num_splits: the chunked plan's unit budget
     int unit_cap;        // partial slots in the workspace (>= units and >= rows + kMaxPairs - 1)
     uint64_t wait_ns;    // limit of every pipeline wait (smla_set_wait_limit_ns; default 2 s)
+    int pair;            // 1: rows 2v and 2v+1 share a work row (num_heads <= 64), else 0
+    int vrows;           // work rows: ceil(num_rows / 2) when paired, else num_rows
+    int lanes;           // heads of a partial (its stride): 128 when paired, else num_heads
 };
 
 struct UnitDesc {
@@ -302,22 +306,156 @@ __device__ __forceinline__ long long map_position(const smla_decode_args& a, lon
     return phys < a.n_main ? phys : -1;
 }
 
-// Number of 64-entry tiles of row r.  Its slots are the top-k slots, the
-// window and the compressed entries, each segment padded to 32-entry raw
-// tiles; two raw tiles make a tile (the last one may be half empty).
-__device__ __forceinline__ int row_tiles(const smla_decode_args& a, int r, uint32_t& err) {
-    int t = ceil_div_i(a.topk, kRawBK);
-    if (a.swa_len != nullptr) {
-        int w = __ldg(a.swa_len + r);
-        if (w < 0) { err |= SMLA_DEV_BAD_LENGTH; w = 0; }
-        t += ceil_div_i(w, kRawBK);
+// A work row.  With num_heads <= 64 two rows share one: rows A = 2v and
+// B = 2v + 1 (B absent when num_rows is odd) take TMEM lanes [0, 64) and
+// [64, 128), and the MMA's M = 128 is filled by both.  Its slots, each
+// segment padded to 32-entry raw tiles:
+//   A's top-k slots; B's top-k slots;
+//   the window: the union of A's and B's windows when both read the same
+//     sequence, else A's window then B's;
+//   the compressed entries: the union when both start at the same compressed
+//     row, else A's then B's.
+// Each slot is valid for A, for B or both (a position inside both windows, a
+// compressed entry below both lengths).  Without pairing the work row is the
+// row itself (B absent) and its slots are exactly the row's.  Two rows of a
+// multi-token decode of one sequence share nearly all of their window and
+// compressed entries, which are then gathered and multiplied once.
+struct VRow {
+    int rA, rB;             // rows (rB = -1: absent)
+    int seqA, seqB;
+    int nmt;                // raw tiles of one row's top-k
+    int wsA, wlA, wsB, wlB; // windows: start and length per row
+    int w0, wn;             // the union window (wu)
+    long long csA, csB;     // compressed: first row per row
+    int clA, clB, cn;       // lengths, and the union's (cu)
+    bool wu, cu;
+    int nA, nB, nW, nC;     // raw tiles of the four segments
+};
+
+__device__ __forceinline__ VRow make_vrow(const KParams& p, int v, uint32_t& err) {
+    const smla_decode_args& a = p.a;
+    VRow w;
+    w.rA = p.pair ? 2 * v : v;
+    w.rB = (p.pair && 2 * v + 1 < a.num_rows) ? 2 * v + 1 : -1;
+    w.seqA = a.row_seq != nullptr ? __ldg(a.row_seq + w.rA) : w.rA;
+    w.seqB = w.rB < 0 ? -1 : (a.row_seq != nullptr ? __ldg(a.row_seq + w.rB) : w.rB);
+    w.nmt = ceil_div_i(a.topk, kRawBK);
+    auto win = [&](int r, int& st, int& ln) {
+        st = 0; ln = 0;
+        if (r < 0 || a.swa_len == nullptr) return;
+        ln = __ldg(a.swa_len + r);
+        if (ln < 0) { err |= SMLA_DEV_BAD_LENGTH; ln = 0; }
+        st = __ldg(a.swa_start + r);
+    };
+    auto cmpr = [&](int r, long long& st, int& ln) {
+        st = 0; ln = 0;
+        if (r < 0 || a.cmp_len == nullptr) return;
+        ln = __ldg(a.cmp_len + r);
+        if (ln < 0) { err |= SMLA_DEV_BAD_LENGTH; ln = 0; }
+        st = __ldg(a.cmp_start + r);
+    };
+    win(w.rA, w.wsA, w.wlA);
+    win(w.rB, w.wsB, w.wlB);
+    cmpr(w.rA, w.csA, w.clA);
+    cmpr(w.rB, w.csB, w.clB);
+    w.wu = w.rB >= 0 && w.seqA == w.seqB && w.wlA > 0 && w.wlB > 0;
+    if (w.wu) {
+        w.w0 = min(w.wsA, w.wsB);
+        w.wn = max(w.wsA + w.wlA, w.wsB + w.wlB) - w.w0;
+        // a union longer than the two windows laid end to end saves nothing
+        if (w.wn > w.wlA + w.wlB) w.wu = false;
     }
-    if (a.cmp_len != nullptr) {
-        int c = __ldg(a.cmp_len + r);
-        if (c < 0) { err |= SMLA_DEV_BAD_LENGTH; c = 0; }
-        t += ceil_div_i(c, kRawBK);
+    w.cu = w.rB >= 0 && w.csA == w.csB && w.clA > 0 && w.clB > 0;
+    w.cn = w.cu ? max(w.clA, w.clB) : 0;
+    w.nA = w.nmt;
+    w.nB = w.rB >= 0 ? w.nmt : 0;
+    w.nW = w.wu ? ceil_div_i(w.wn, kRawBK) : ceil_div_i(w.wlA, kRawBK) + ceil_div_i(w.wlB, kRawBK);
+    w.nC = w.cu ? ceil_div_i(w.cn, kRawBK) : ceil_div_i(w.clA, kRawBK) + ceil_div_i(w.clB, kRawBK);
+    return w;
+}
+
+// Number of 64-entry tiles of a work row (two raw tiles per tile; the last
+// one may be half empty).
+__device__ __forceinline__ int vrow_tiles(const VRow& w) { return ceil_div_i(w.nA + w.nB + w.nW + w.nC, kRawPerTile); }
+
+// Slot `lane` of raw tile t of a work row: the pool row (phys >= 0, in the
+// compressed pool when *cmp), and for which of A, B it counts.
+__device__ __forceinline__ long long vrow_slot(const smla_decode_args& a, const VRow& w, int t, int lane, bool& cmp,
+                                               bool& vA, bool& vB, uint32_t& err) {
+    long long phys = -1;
+    cmp = false;
+    vA = vB = false;
+    if (t < w.nA + w.nB) {  // top-k of A, then of B
+        const bool isB = t >= w.nA;
+        const int r = isB ? w.rB : w.rA;
+        const int j = (isB ? t - w.nA : t) * kRawBK + lane;
+        if (j < a.topk) {
+            const int idx = __ldg(a.main_idx + (size_t)r * a.topk + j);
+            if (idx != -1) {
+                phys = map_position(a, idx, isB ? w.seqB : w.seqA);
+                if (phys < 0) err |= SMLA_DEV_BAD_INDEX;
+                else { vA = !isB; vB = isB; }
+            }
+        }
+        return phys;
     }
-    return ceil_div_i(t, kRawPerTile);
+    t -= w.nA + w.nB;
+    if (t < w.nW) {  // window
+        long long pos;
+        int seq;
+        if (w.wu) {
+            const int j = t * kRawBK + lane;
+            if (j >= w.wn) return -1;
+            pos = (long long)w.w0 + j;
+            vA = pos >= w.wsA && pos < (long long)w.wsA + w.wlA;
+            vB = pos >= w.wsB && pos < (long long)w.wsB + w.wlB;
+            seq = w.seqA;
+        } else {
+            const int tA = ceil_div_i(w.wlA, kRawBK);
+            const bool isB = t >= tA;
+            const int j = (isB ? t - tA : t) * kRawBK + lane;
+            if (j >= (isB ? w.wlB : w.wlA)) return -1;
+            pos = (long long)(isB ? w.wsB : w.wsA) + j;
+            vA = !isB;
+            vB = isB;
+            seq = isB ? w.seqB : w.seqA;
+        }
+        phys = map_position(a, pos, seq);
+        if (phys < 0) {
+            err |= SMLA_DEV_BAD_INDEX;
+            vA = vB = false;
+        }
+        return phys;
+    }
+    t -= w.nW;
+    if (t < w.nC) {  // compressed entries
+        long long start;
+        int j;
+        if (w.cu) {
+            j = t * kRawBK + lane;
+            if (j >= w.cn) return -1;
+            start = w.csA;
+            vA = j < w.clA;
+            vB = j < w.clB;
+        } else {
+            const int tA = ceil_div_i(w.clA, kRawBK);
+            const bool isB = t >= tA;
+            j = (isB ? t - tA : t) * kRawBK + lane;
+            if (j >= (isB ? w.clB : w.clA)) return -1;
+            start = isB ? w.csB : w.csA;
+            vA = !isB;
+            vB = isB;
+        }
+        cmp = true;
+        phys = start + j;
+        if (phys < 0 || phys >= a.n_cmp) {
+            err |= SMLA_DEV_BAD_CMP;
+            phys = -1;
+            vA = vB = false;
+        }
+        return phys;
+    }
+    return -1;
 }
 
 // Per-CTA state shared by the roles.
@@ -424,47 +562,14 @@ __device__ void producer_role(const KParams& p, const Ctx& c, const UnitDesc* un
     };
     for (int ui = 0; ui < n_units; ++ui) {
         const UnitDesc d = units[ui];
-        const int r = d.row;
-        const int seq = a.row_seq != nullptr ? __ldg(a.row_seq + r) : r;
-        const int nmt = ceil_div_i(a.topk, kRawBK);
-        int swa_len = 0, swa_start = 0, cmp_len = 0;
-        long long cmp_start = 0;
-        if (a.swa_len != nullptr) { swa_len = max(0, __ldg(a.swa_len + r)); swa_start = __ldg(a.swa_start + r); }
-        if (a.cmp_len != nullptr) { cmp_len = max(0, __ldg(a.cmp_len + r)); cmp_start = __ldg(a.cmp_start + r); }
-        const int nst = ceil_div_i(swa_len, kRawBK);
-        const int nct = ceil_div_i(cmp_len, kRawBK);
+        const VRow w = make_vrow(p, d.row, err);
         for (int t = kRawPerTile * d.t_begin; t < kRawPerTile * d.t_end; ++t, ++q) {
             if ((int)(q % kNR) != pw) continue;
             const uint32_t rs = q % kNR, rph = (q / kNR) & 1u;
             // resolve this lane's slot (raw tiles past the row's end stay empty)
-            long long phys = -1;
-            bool cmp = false;
-            if (t < nmt) {
-                const int j = t * kRawBK + lane;
-                if (j < a.topk) {
-                    const int idx = __ldg(a.main_idx + (size_t)r * a.topk + j);
-                    if (idx != -1) {
-                        phys = map_position(a, idx, seq);
-                        if (phys < 0) err |= SMLA_DEV_BAD_INDEX;
-                    }
-                }
-            } else if (t < nmt + nst) {
-                const int j = (t - nmt) * kRawBK + lane;
-                if (j < swa_len) {
-                    phys = map_position(a, (long long)swa_start + j, seq);
-                    if (phys < 0) err |= SMLA_DEV_BAD_INDEX;
-                }
-            } else if (t < nmt + nst + nct) {
-                const int j = (t - nmt - nst) * kRawBK + lane;
-                if (j < cmp_len) {
-                    cmp = true;
-                    phys = cmp_start + j;
-                    if (phys < 0 || phys >= a.n_cmp) {
-                        err |= SMLA_DEV_BAD_CMP;
-                        phys = -1;
-                    }
-                }
-            }
+            bool cmp, vA, vB;
+            long long phys = vrow_slot(a, w, t, lane, cmp, vA, vB, err);
+            if (!(vA || vB)) phys = -1;
             const uint8_t* ep = nullptr;
             const uint8_t* sp = nullptr;
             if (phys >= 0) {
@@ -514,9 +619,13 @@ __device__ void producer_role(const KParams& p, const Ctx& c, const UnitDesc* un
             }
             if (ep != nullptr) cp_async_8(c.sb + kOffRawSc + (rs * kRawBK + lane) * 8, sp);
             cp_async_arrive_noinc(full);  // one of the 32 async arrivals
+            const uint32_t maskA = __ballot_sync(0xffffffffu, vA && ep != nullptr);
+            const uint32_t maskB = p.pair ? __ballot_sync(0xffffffffu, vB && ep != nullptr) : maskA;
             if (lane == 0) {
-                st_shared_u32(c.sb + kOffRawMask + rs * 4, mask);
-                mbar_arrive_local(full);  // the 33rd arrival, ordered after the mask store
+                st_shared_u32(c.sb + kOffRawMask + rs * 16, mask);
+                st_shared_u32(c.sb + kOffRawMask + rs * 16 + 4, maskA);
+                st_shared_u32(c.sb + kOffRawMask + rs * 16 + 8, maskB);
+                mbar_arrive_local(full);  // the 33rd arrival, ordered after the mask stores
             }
             last_fill = (int64_t)q;
         }
@@ -540,8 +649,15 @@ __device__ void producer_role(const KParams& p, const Ctx& c, const UnitDesc* un
 //          warps 4-7 fp8 (atom 5, group dw-4) and RoPE tasks 2(dw-4), 2(dw-4)+1.
 // A set is written to the 4-atom buffer `dst` (local atom = atom % 4).
 // Returns, when `bound` is set, a bound on |x| over the values written.
+// With `bound` (the own dims, which PV reads) a chunk that holds a NaN or an
+// infinity, of an entry that only one row of a paired work row selects (maskA
+// != maskB there), is stored as zeros: the other row must get exactly 0 from
+// an entry it does not select, and 0 x NaN is NaN.  The selecting row is
+// reported in *poison (bit 0 row A, bit 1 row B) and its outputs become NaN,
+// as that row's own arithmetic would have made them.
 __device__ __forceinline__ float dequant_set(uint32_t raw, uint32_t rawsc, uint32_t dst, int row0, uint32_t mask,
-                                             int set, int dw, int lane, bool bound) {
+                                             uint32_t maskA, uint32_t maskB, int set, int dw, int lane, bool bound,
+                                             uint32_t& poison) {
     const int ef = 8 * (dw & 3) + (lane >> 2);  // entry of this warp's fp8 tasks
     const bool fvalid = (mask >> (ef & 31)) & 1u;
     int atom[2];
@@ -592,8 +708,18 @@ __device__ __forceinline__ float dequant_set(uint32_t raw, uint32_t rawsc, uint3
     if (has_rope) {
 #pragma unroll
         for (int it = 0; it < 2; ++it) {
-            if (bound) vbound = fmaxf(vbound, bf16x8_absmax(rv[it]));
-            st_shared_v4(dst + 3 * kAtomBytes + sw128_offset(row0 + er[it], kr), rv[it].x, rv[it].y, rv[it].z, rv[it].w);
+            uint4 rvv = rv[it];
+            if (bound) {
+                const float ab = bf16x8_absmax(rvv);
+                const uint32_t eb = 1u << (er[it] & 31);
+                if (ab == INFINITY && ((maskA ^ maskB) & eb)) {  // non-finite, one row only
+                    poison |= (maskA & eb) ? 1u : 2u;
+                    rvv = make_uint4(0u, 0u, 0u, 0u);
+                } else {
+                    vbound = fmaxf(vbound, ab);
+                }
+            }
+            st_shared_v4(dst + 3 * kAtomBytes + sw128_offset(row0 + er[it], kr), rvv.x, rvv.y, rvv.z, rvv.w);
         }
     }
     if (__any_sync(0xffffffffu, bad[0] || bad[1])) {  // rare: one copy of the exact path
@@ -607,7 +733,14 @@ __device__ __forceinline__ float dequant_set(uint32_t raw, uint32_t rawsc, uint3
             uint32_t o[8];
             dequant16(vv, scale, o);
             const float bnd = e4m3x16_absmax(vv) * scale;
-            vbound = (bnd > vbound || bnd != bnd) ? (bnd != bnd ? INFINITY : bnd) : vbound;
+            const uint32_t eb = 1u << (ef & 31);
+            if (bound && !(bnd < INFINITY) && ((maskA ^ maskB) & eb)) {  // non-finite, one row only
+                poison |= (maskA & eb) ? 1u : 2u;
+#pragma unroll
+                for (int z = 0; z < 8; ++z) o[z] = 0u;
+            } else {
+                vbound = (bnd > vbound || bnd != bnd) ? (bnd != bnd ? INFINITY : bnd) : vbound;
+            }
             const uint32_t d = dst + ((it == 0 ? atom[0] : atom[1]) & 3) * kAtomBytes;
             st_shared_v4(d + sw128_offset(row0 + ef, kk), o[0], o[1], o[2], o[3]);
             st_shared_v4(d + sw128_offset(row0 + ef, kk + 1), o[4], o[5], o[6], o[7]);
@@ -628,7 +761,8 @@ __device__ void dequant_role(const Ctx& c, const UnitDesc* units, int n_units, i
         const int n = units[ui].t_end - units[ui].t_begin;
         for (int i = 0; i < n; ++i, ++g) {
             const uint32_t xs = g % kNXO;
-            uint32_t mask0 = 0u, mask1 = 0u;
+            uint32_t mask0 = 0u, mask1 = 0u, mab = 0u;  // mab: this lane's (raw tile, A/B) mask, lanes 0..3
+            uint32_t mA[kRawPerTile] = {0u, 0u}, mB[kRawPerTile] = {0u, 0u}, poison = 0u;
             float vbound = 0.f;
 #pragma unroll 1
             for (int step = 0; step < 2 * kRawPerTile; ++step) {
@@ -638,8 +772,11 @@ __device__ void dequant_role(const Ctx& c, const UnitDesc* units, int n_units, i
                 const uint32_t rs = q % kNR;
                 if (!own) {
                     if (!wait_bar_warp(c, bar_addr(c, BAR_RAW_FULL + rs), (q / kNR) & 1u)) return;
-                    const uint32_t m = ld_shared_u32(c.sb + kOffRawMask + rs * 4);
+                    const uint32_t m = ld_shared_u32(c.sb + kOffRawMask + rs * 16);
                     if (k == 0) mask0 = m; else mask1 = m;
+                    if ((lane >> 1) == k && lane < 4) mab = ld_shared_u32(c.sb + kOffRawMask + rs * 16 + 4 + 4 * (lane & 1));
+                    mA[k] = ld_shared_u32(c.sb + kOffRawMask + rs * 16 + 4);
+                    mB[k] = ld_shared_u32(c.sb + kOffRawMask + rs * 16 + 8);
                     if (k == 0 && !wait_bar_warp(c, bar_addr(c, BAR_XP_EMPTY), (g & 1u) ^ 1u)) return;
                 } else if (k == 0) {
                     fence_proxy_async_smem();
@@ -650,17 +787,19 @@ __device__ void dequant_role(const Ctx& c, const UnitDesc* units, int n_units, i
                 const uint32_t dst = own ? c.sb + kOffXO + xs * kHalfBytes : c.sb + kOffXP;
                 const int set = own ? (int)c.half : 1 - (int)c.half;
                 vbound = fmaxf(vbound, dequant_set(c.sb + kOffRaw + rs * kRawStageBytes, c.sb + kOffRawSc + rs * kRawBK * 8,
-                                                   dst, kRawBK * k, k == 0 ? mask0 : mask1, set, dw, lane, own));
+                                                   dst, kRawBK * k, k == 0 ? mask0 : mask1, mA[k], mB[k], set, dw, lane,
+                                                   own, poison));
                 if (own) {
                     __syncwarp();
                     if (lane == 0) mbar_arrive_local(bar_addr(c, BAR_RAW_EMPTY + rs));
                 }
             }
-            if (dw == 0 && lane < kRawPerTile)
-                st_shared_u32(c.sb + kOffXMask + (xs * kRawPerTile + lane) * 4, lane == 0 ? mask0 : mask1);
+            if (dw == 0 && lane < 2 * kRawPerTile) st_shared_u32(c.sb + kOffXMask + (xs * 4 + lane) * 4, mab);
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) vbound = fmaxf(vbound, __shfl_xor_sync(0xffffffffu, vbound, o));
             if (lane == 0) st_shared_f32(c.sb + kOffXVmax + (xs * kNumDequantWarps + dw) * 4, vbound);
+            poison = __reduce_or_sync(0xffffffffu, poison);
+            if (lane == 0) st_shared_u32(c.sb + kOffXPoison + (xs * kNumDequantWarps + dw) * 4, poison);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive_local(bar_addr(c, BAR_X_FULL + xs));
@@ -764,15 +903,16 @@ __device__ void mma_role(const Ctx& c, const UnitDesc* units, int n_units) {
 __device__ __forceinline__ uint32_t stage_addr(const Ctx& c, int h, int chunk) {
     return c.sb + kOffQ + (uint32_t)h * 512u + (uint32_t)((chunk ^ (h & 31)) * 16);
 }
-// Write this warp's 32 staged rows: row h (h < H) to dst_row(h) (512 bytes).
-template <class RowPtr>
-__device__ __forceinline__ void stage_flush(const Ctx& c, int warp, int lane, int H, RowPtr dst_row) {
+// Write this warp's 32 staged rows: lane h's row (when keep(h)) to dst_row(h)
+// (512 bytes).
+template <class Keep, class RowPtr>
+__device__ __forceinline__ void stage_flush(const Ctx& c, int warp, int lane, Keep keep, RowPtr dst_row) {
     __syncwarp();
 #pragma unroll 4
     for (int rr = 0; rr < 32; ++rr) {
         const int h = 32 * warp + rr;
         const uint4 v = ld_shared_v4(stage_addr(c, h, lane));
-        if (h < H) __stcg(reinterpret_cast<uint4*>(dst_row(h)) + lane, v);
+        if (keep(h)) __stcg(reinterpret_cast<uint4*>(dst_row(h)) + lane, v);
     }
     __syncwarp();
 }
@@ -790,13 +930,21 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, UnitDesc* units, in
     const int H = a.num_heads;
     const uint32_t lane_base = (uint32_t)(qw * 32) << 16;
     const float qscale = a.sm_scale * kLog2e;
-    const float sink2 = (a.sink != nullptr && h < H) ? __ldg(a.sink + h) * kLog2e : -INFINITY;
+    // Lane -> (row of the work row, head): paired work rows put row A on lanes
+    // 0..63 and row B on 64..127; lanes past num_heads are padding.
+    const int sub = p.pair ? (h >> 6) : 0;       // 0 = row A, 1 = row B
+    const int hr = p.pair ? (h & 63) : h;        // head within its row
+    const float sink2 = (a.sink != nullptr && hr < H) ? __ldg(a.sink + hr) * kLog2e : -INFINITY;
     uint32_t g = 0;
     bool ok = true;
 
     for (int ui = 0; ui < n_units && ok; ++ui) {
         const UnitDesc d = units[ui];
-        const int r = d.row;
+        const int rA = p.pair ? 2 * d.row : d.row;
+        const int rB = (p.pair && rA + 1 < a.num_rows) ? rA + 1 : -1;
+        const int row_of_sub[2] = {rA, rB};
+        const int r = row_of_sub[sub];                  // this lane's row (-1: absent)
+        const bool live = hr < H && r >= 0;              // this lane carries a real head
         const int n = d.t_end - d.t_begin;
         // ---- Q of this row (side 0): its peer dims (the 256 this CTA does not
         //      output) -> TMEM [384, 512) as bf16 pairs, its own dims -> shared
@@ -804,11 +952,13 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, UnitDesc* units, in
         //      are prefetched into L2 now, a unit ahead.
         if (sd == 0) {
             if (h == 0 && ui + 1 < n_units) {
-                const size_t rn = (size_t)units[ui + 1].row * H;
+                const int rn0 = p.pair ? 2 * units[ui + 1].row : units[ui + 1].row;
+                const int nr = (p.pair && rn0 + 1 < a.num_rows) ? 2 : 1;  // rows of a work row are adjacent
+                const size_t rn = (size_t)rn0 * H;
                 bulk_prefetch_l2(static_cast<const uint16_t*>(a.q_nope) + rn * SMLA_NOPE_DIMS,
-                                 (uint32_t)(H * SMLA_NOPE_DIMS * 2));
+                                 (uint32_t)(nr * H * SMLA_NOPE_DIMS * 2));
                 bulk_prefetch_l2(static_cast<const uint16_t*>(a.q_rope) + rn * SMLA_ROPE_DIMS,
-                                 (uint32_t)(H * SMLA_ROPE_DIMS * 2));
+                                 (uint32_t)(nr * H * SMLA_ROPE_DIMS * 2));
             }
             // Q in 16-byte chunks j = dims 8j .. 8j + 7 (NoPE chunks 0..55, RoPE
             // 56..63).  Each warp copies its 32 heads one head per instruction
@@ -818,21 +968,25 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, UnitDesc* units, in
             // 32 chunks go straight to their place in the Q region, K-major with
             // the 128-byte swizzle (after every warp has read its staged rows).
             // Heads beyond num_heads are zero-filled.
-            const uint4* qn = static_cast<const uint4*>(a.q_nope) + (size_t)r * H * (SMLA_NOPE_DIMS / 8);
-            const uint4* qr = static_cast<const uint4*>(a.q_rope) + (size_t)r * H * (SMLA_ROPE_DIMS / 8);
+            const uint4* qn = static_cast<const uint4*>(a.q_nope);
+            const uint4* qr = static_cast<const uint4*>(a.q_rope);
             const int pbase = 32 * (1 - (int)c.half), obase = 32 * (int)c.half;
+            // lane hh's (row, head): this warp's 32 lanes all belong to one row
+            const int wr = row_of_sub[p.pair ? (warp >> 1) : 0];
 #pragma unroll 1
             for (int pass = 0; pass < 2; ++pass) {
                 const int j = (pass == 0 ? pbase : obase) + lane;
 #pragma unroll 8
                 for (int rr = 0; rr < 32; ++rr) {
                     const int hh = 32 * warp + rr;
-                    const int hs = hh < H ? hh : 0;
-                    const uint4* src = j < 56 ? qn + (size_t)hs * (SMLA_NOPE_DIMS / 8) + j
-                                              : qr + (size_t)hs * (SMLA_ROPE_DIMS / 8) + (j - 56);
+                    const int hd = p.pair ? (hh & 63) : hh;
+                    const bool real = hd < H && wr >= 0;
+                    const size_t qrow = real ? (size_t)wr * H + hd : 0;
+                    const uint4* src = j < 56 ? qn + qrow * (SMLA_NOPE_DIMS / 8) + j
+                                              : qr + qrow * (SMLA_ROPE_DIMS / 8) + (j - 56);
                     const uint32_t dst = pass == 0 ? stage_addr(c, hh, lane)
                                                    : c.sb + kOffQ + (lane >> 3) * 16384 + sw128_offset(hh, lane & 7);
-                    cp_async_16(dst, src, hh < H ? 16u : 0u);
+                    cp_async_16(dst, src, real ? 16u : 0u);
                 }
                 cp_async_wait_all();
                 __syncwarp();
@@ -860,6 +1014,7 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, UnitDesc* units, in
         float m_used = -INFINITY, lsum = 0.f;
         float skipped = 0.f;  // bound on the lo-half contributions skipped so far (units of lsum)
         bool o_init = false;
+        bool poisoned = false;  // an entry this row selects held a NaN / inf stored as zeros (dequant_set)
         // QK's peer-dims partial of this side's 32 columns of the tile about to
         // be processed (see mma_role): taken into registers, which frees the
         // columns for the own-dims chain.
@@ -895,7 +1050,9 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, UnitDesc* units, in
             if (ok && !wait_bar_warp(c, bar_addr(c, BAR_S_FULL + sbuf), (g >> 1) & 1u)) ok = false;
             if (ok && !wait_bar_warp(c, bar_addr(c, BAR_X_FULL + xs), (g / kNXO) & 1u)) ok = false;
             tc_fence_after();
-            const uint32_t vm = ld_shared_u32(c.sb + kOffXMask + (xs * kRawPerTile + sd) * 4);
+            // this side's 32 entries, valid for this warp's row (quarters 2, 3
+            // hold row B of a paired work row; without pairing both masks agree)
+            const uint32_t vm = ld_shared_u32(c.sb + kOffXMask + (xs * 4 + 2 * sd + (qw >> 1)) * 4);
             // pass 1: this side's scores (own-dims chain + peer-dims partial, added
             // in fp32 and written back for pass 2) and their masked maximum (taken
             // over the raw scores: qscale > 0)
@@ -938,12 +1095,17 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, UnitDesc* units, in
             // sum.  Both sides take the same decision from the same values.
             const uint32_t vb = c.sb + kOffXVmax + xs * (4 * kNumDequantWarps);
             float vmax = ld_shared_f32(vb);
+            uint32_t pois = ld_shared_u32(c.sb + kOffXPoison + xs * (4 * kNumDequantWarps));
 #pragma unroll
-            for (int w = 1; w < kNumDequantWarps; ++w) vmax = fmaxf(vmax, ld_shared_f32(vb + 4 * w));
+            for (int w = 1; w < kNumDequantWarps; ++w) {
+                vmax = fmaxf(vmax, ld_shared_f32(vb + 4 * w));
+                pois |= ld_shared_u32(c.sb + kOffXPoison + (xs * kNumDequantWarps + w) * 4);
+            }
+            if (ok && ((pois >> sub) & 1u)) poisoned = true;
             const float capk = 32.f * (1.0f / 512.0f) * (1.0f + 1.0f / 256.0f);
             const float cap0 = mt0 == -INFINITY ? 0.f : capk * ex2_approx(mt0 - msub);
             const float cap1 = mt1 == -INFINITY ? 0.f : capk * ex2_approx(mt1 - msub);
-            const bool cold = __all_sync(0xffffffffu, (h >= H) || (skipped * alpha + (cap0 + cap1) * vmax <= kLoBudget * lsum * alpha));
+            const bool cold = __all_sync(0xffffffffu, !live || (skipped * alpha + (cap0 + cap1) * vmax <= kLoBudget * lsum * alpha));
             // The next tile's peer partial is taken now (this tile's scores are
             // back in TMEM), so that QK's own-dims chain of the next tile runs
             // while this tile's P is computed.
@@ -1025,7 +1187,7 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, UnitDesc* units, in
             // bounds what skipping drops; both sides reach the same vote
             {
                 const float cand = skipped + lo_abs * vmax;
-                const bool mine = (h >= H) || cold || (cand <= kLoBudget * lsum);
+                const bool mine = !live || cold || (cand <= kLoBudget * lsum);
                 const bool warp_ok = __all_sync(0xffffffffu, mine);
                 if (warp_ok) skipped = cand;  // counted even if another quarter vetoes: conservative
                 if (sd == 0 && lane == 0) st_shared_u32(c.sb + kOffVote + (sbuf * 4 + qw) * 4, warp_ok ? 1u : 0u);
@@ -1047,6 +1209,7 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, UnitDesc* units, in
         }
         if (sd != 0) continue;  // side 0 finishes the unit and stages the next Q
         tc_fence_after();       // side 1's rescales of O are complete (before the barrier)
+        if (poisoned) { m_used = NAN; lsum = NAN; }  // the row's partial or outputs become NaN, as a selected NaN makes them
         // ---- finish: final bf16 output, or an fp32 partial for the merge kernel ----
         if (d.s_r == 1) {
             const float M = fmaxf(m_used, sink2);
@@ -1058,7 +1221,8 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, UnitDesc* units, in
                 oscale = Z > 0.f ? wm / Z : 0.f;
                 lse = (M + log2f(Z)) * kLn2;
             }
-            if (lsum == 0.f) lse = (a.sink != nullptr && h < H) ? __ldg(a.sink + h) : -INFINITY;  // sink only, exactly
+            if (lsum == 0.f) lse = (a.sink != nullptr && hr < H) ? __ldg(a.sink + hr) : -INFINITY;  // sink only, exactly
+            if (poisoned) { oscale = NAN; lse = NAN; }
             // 256 bf16 dims per head = one 512-byte staged row
 #pragma unroll 1
             for (int cc = 0; cc < 8; ++cc) {
@@ -1078,10 +1242,15 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, UnitDesc* units, in
                                  pack_bf16(__uint_as_float(v[8 * q + 4]) * oscale, __uint_as_float(v[8 * q + 5]) * oscale),
                                  pack_bf16(__uint_as_float(v[8 * q + 6]) * oscale, __uint_as_float(v[8 * q + 7]) * oscale));
             }
-            stage_flush(c, warp, lane, H, [&](int hh) {
-                return static_cast<uint16_t*>(a.out) + ((size_t)r * H + hh) * SMLA_HEAD_DIM + 256 * c.half;
-            });
-            if (c.half == 0 && a.lse != nullptr && h < H) a.lse[(size_t)r * H + h] = lse;
+            {
+                const int wr = row_of_sub[p.pair ? (warp >> 1) : 0];  // the row of this warp's 32 lanes
+                stage_flush(c, warp, lane, [&](int hh) { return (p.pair ? (hh & 63) : hh) < H && wr >= 0; },
+                            [&](int hh) {
+                                return static_cast<uint16_t*>(a.out) +
+                                       ((size_t)wr * H + (p.pair ? (hh & 63) : hh)) * SMLA_HEAD_DIM + 256 * c.half;
+                            });
+            }
+            if (c.half == 0 && a.lse != nullptr && live) a.lse[(size_t)r * H + hr] = lse;
         } else {
             const size_t ub = (size_t)d.unit;
             // 256 fp32 dims per head: two passes of 128 dims (one 512-byte staged row)
@@ -1096,9 +1265,10 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, UnitDesc* units, in
                     for (int q = 0; q < 8; ++q)
                         st_shared_v4(stage_addr(c, h, 8 * cc + q), v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
                 }
-                stage_flush(c, warp, lane, H, [&](int hh) { return p.po + ((ub * 2 + c.half) * H + hh) * 256 + 128 * hf; });
+                stage_flush(c, warp, lane, [&](int hh) { return (p.pair ? (hh & 63) : hh) < H; },
+                            [&](int hh) { return p.po + ((ub * 2 + c.half) * p.lanes + hh) * 256 + 128 * hf; });
             }
-            if (h < H) __stcg(p.ml + (ub * 2 + c.half) * H + h, make_float2(m_used, lsum));
+            if (hr < H) __stcg(p.ml + (ub * 2 + c.half) * p.lanes + h, make_float2(m_used, lsum));
         }
         // All TMEM reads of O are complete (tcgen05.wait::ld) before the next
         // unit's Q is staged; its first PV (which overwrites O) waits for Q.
@@ -1189,11 +1359,11 @@ __device__ void plan_warp(const KParams& p, int pair, int n_pairs, UnitDesc* uni
                           int* s_tiles, int* s_prefix, int* s_cum, int* s_cut, int* s_eacc, uint32_t& plan_err) {
     const smla_decode_args& a = p.a;
     const int lane = threadIdx.x & 31;
-    const int R = a.num_rows;
+    const int R = p.vrows;  // work rows
     const int budget = max(R, p.units > n_pairs ? (p.units / n_pairs) * n_pairs : p.units);
     int max_t = 1;
     for (int r = lane; r < R; r += 32) {
-        const int t = row_tiles(a, r, plan_err);
+        const int t = vrow_tiles(make_vrow(p, r, plan_err));
         s_tiles[r] = t;
         max_t = max(max_t, t);
     }
@@ -1357,11 +1527,13 @@ __device__ void plan_warp(const KParams& p, int pair, int n_pairs, UnitDesc* uni
         }
         misc[2] = (uint32_t)n;
         if (n > 0) {  // the first unit's q rows start their trip to L2 now
-            const size_t r0 = (size_t)units[0].row * a.num_heads;
+            const int rr0 = p.pair ? 2 * units[0].row : units[0].row;
+            const int nr = (p.pair && rr0 + 1 < a.num_rows) ? 2 : 1;
+            const size_t r0 = (size_t)rr0 * a.num_heads;
             bulk_prefetch_l2(static_cast<const uint16_t*>(a.q_nope) + r0 * SMLA_NOPE_DIMS,
-                             (uint32_t)(a.num_heads * SMLA_NOPE_DIMS * 2));
+                             (uint32_t)(nr * a.num_heads * SMLA_NOPE_DIMS * 2));
             bulk_prefetch_l2(static_cast<const uint16_t*>(a.q_rope) + r0 * SMLA_ROPE_DIMS,
-                             (uint32_t)(a.num_heads * SMLA_ROPE_DIMS * 2));
+                             (uint32_t)(nr * a.num_heads * SMLA_ROPE_DIMS * 2));
         }
     }
     __syncwarp();
@@ -1485,14 +1657,16 @@ constexpr int kMergeThreads = 32 * kMergeHeads;
 
 __global__ void __launch_bounds__(kMergeThreads) smla_merge_kernel(const KParams p) {
     const smla_decode_args& a = p.a;
-    const int r = blockIdx.x, half = blockIdx.y, H = a.num_heads;
-    const int h = blockIdx.z * kMergeHeads + (int)(threadIdx.x >> 5), q = threadIdx.x & 31;
-    const int2 rt = p.row_table[r];
+    const int v = blockIdx.x, half = blockIdx.y, H = a.num_heads, Lw = p.lanes;
+    const int lh = blockIdx.z * kMergeHeads + (int)(threadIdx.x >> 5), q = threadIdx.x & 31;  // lane of the work row
+    const int2 rt = p.row_table[v];
     const int u0 = rt.x, sr = rt.y;
-    if (sr <= 1 || h >= H) return;
-    const size_t ml_step = 2 * (size_t)H, po_step = 2 * (size_t)H * 256;  // one unit
-    const float2* ml = p.ml + ((size_t)u0 * 2 + half) * H + h;
-    const float* po = p.po + (((size_t)u0 * 2 + half) * H + h) * 256 + 8 * q;
+    const int r = p.pair ? 2 * v + (lh >> 6) : v;  // the row and head this lane holds
+    const int h = p.pair ? (lh & 63) : lh;
+    if (sr <= 1 || lh >= Lw || h >= H || r >= a.num_rows) return;
+    const size_t ml_step = 2 * (size_t)Lw, po_step = 2 * (size_t)Lw * 256;  // one unit
+    const float2* ml = p.ml + ((size_t)u0 * 2 + half) * Lw + lh;
+    const float* po = p.po + (((size_t)u0 * 2 + half) * Lw + lh) * 256 + 8 * q;
     const float sink2 = a.sink != nullptr ? __ldg(a.sink + h) * kLog2e : -INFINITY;
     float M = sink2, Z = sink2 != -INFINITY ? 1.f : 0.f, lall = 0.f;
     float acc[8];
@@ -1567,8 +1741,11 @@ smla_status launch_decode(const smla_decode_args* args, void* workspace, cudaStr
     kp.row_table = reinterpret_cast<int2*>(ws + L.off_rows);
     kp.ml = reinterpret_cast<float2*>(ws + L.off_ml);
     kp.po = reinterpret_cast<float*>(ws + L.off_po);
-    kp.units = args->num_rows * args->num_splits;
-    kp.unit_cap = unit_capacity(args->num_rows, args->num_splits);
+    kp.pair = pair_rows(args->num_heads) ? 1 : 0;
+    kp.vrows = work_rows(args->num_rows, args->num_heads);
+    kp.lanes = partial_lanes(args->num_heads);
+    kp.units = kp.vrows * args->num_splits;
+    kp.unit_cap = unit_capacity(kp.vrows, args->num_splits);
     kp.wait_ns = wait_limit_ns();
     // Persistent grid: CTA pairs (one CTA per output half) up to what is
     // co-resident (the stream plan can use every one of them), and enough
@@ -1580,7 +1757,7 @@ smla_status launch_decode(const smla_decode_args* args, void* workspace, cudaStr
     smla_decode_kernel<<<grid, block, kSmemBytes, stream>>>(kp);
     if (cudaGetLastError() != cudaSuccess) return SMLA_ERR_CUDA;
     // split rows: a second launch merges their partials across the whole GPU
-    const dim3 mgrid((unsigned)args->num_rows, 2u, (unsigned)((args->num_heads + kMergeHeads - 1) / kMergeHeads));
+    const dim3 mgrid((unsigned)kp.vrows, 2u, (unsigned)((kp.lanes + kMergeHeads - 1) / kMergeHeads));
     smla_merge_kernel<<<mgrid, kMergeThreads, 0, stream>>>(kp);
     return cudaGetLastError() == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA;
 }

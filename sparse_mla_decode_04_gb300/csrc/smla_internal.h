@@ -28,9 +28,17 @@ inline int unit_capacity(int rows, int splits) {
     return a > b ? a : b;
 }
 
+// With num_heads <= 64 the decode pairs rows 2v and 2v + 1 into one work row
+// of 128 TMEM lanes (row A's heads on lanes 0..63, row B's on 64..127); its
+// partials then hold 128 lanes.
+inline bool pair_rows(int heads) { return heads <= 64; }
+inline int work_rows(int rows, int heads) { return pair_rows(heads) ? (rows + 1) / 2 : rows; }
+inline int partial_lanes(int heads) { return pair_rows(heads) ? 128 : heads; }
+
 inline WorkspaceLayout workspace_layout(int rows, int heads, int splits) {
     WorkspaceLayout L;
-    const size_t units = (size_t)unit_capacity(rows, splits);
+    const size_t units = (size_t)unit_capacity(work_rows(rows, heads), splits);
+    heads = partial_lanes(heads);
     L.off_err = 0;
     L.off_rows = 256;
     L.off_ml = align_up(L.off_rows + sizeof(int32_t) * 2 * SMLA_MAX_ROWS, 256);

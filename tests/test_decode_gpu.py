@@ -375,3 +375,33 @@ def test_wait_limit_runs_out_and_the_next_call_is_clean(cuda_device):
     assert flags & smla.SMLA_DEV_TIMEOUT
     check(p, num_splits=4, workspace=ws, what="after timeouts")
     assert ws.read_error() == 0
+
+
+@pytest.mark.parametrize("case", ["A-only NoPE", "B-only RoPE", "shared window"])
+def test_paired_rows_keep_a_nan_to_the_rows_that_select_it(cuda_device, case):
+    """Two rows of one sequence at 64 heads share a work row (their windows and
+    compressed entries are gathered once).  A NaN in an entry that only one row
+    selects reaches that row alone; one in an entry both select reaches both."""
+    p = I.build_problem(name="pair", seq_lens=[3000], rows=[(0, 2999), (0, 3000)], H=64, topk=256,
+                        invalid_frac=0.05, swa=64, seed=51, device="cuda", row_seq=True)
+    if case == "A-only NoPE":
+        only = sorted(set(_referenced_main_entries(p, 0)) - set(_referenced_main_entries(p, 1)))
+        p.kv_pool[only[2], 40] = 0x7F
+    elif case == "B-only RoPE":
+        only = sorted(set(_referenced_main_entries(p, 1)) - set(_referenced_main_entries(p, 0)))
+        p.kv_pool[only[5], 470:472] = torch.tensor([0xC0, 0x7F], dtype=torch.uint8, device="cuda")  # bf16 NaN
+    else:
+        pos = int(p.swa_start[1].item()) + 3  # inside both windows
+        e = int(p.block_table[0, pos // 64].item()) * 64 + pos % 64
+        p.kv_pool[e, 100] = 0x7F
+    out, lse = run_gpu(p, num_splits=2)
+    ro, rl = run_oracle(p)
+    o = out.float().cpu().numpy().astype(np.float64)
+    l = lse.float().cpu().numpy().astype(np.float64)
+    assert np.isnan(rl).any()
+    assert np.array_equal(np.isnan(o), np.isnan(ro)), "NaN pattern differs from the oracle"
+    assert np.array_equal(np.isnan(l), np.isnan(rl))
+    fin = ~np.isnan(ro)
+    assert (np.abs(o[fin] - ro[fin]) <= 1e-2 + 1e-2 * np.abs(ro[fin])).all()
+    finl = ~np.isnan(rl)
+    assert (np.abs(l[finl] - rl[finl]) <= 1e-3).all()
