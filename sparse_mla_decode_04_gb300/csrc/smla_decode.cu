@@ -619,8 +619,8 @@ __device__ void producer_role(const KParams& p, const Ctx& c, const UnitDesc* un
             }
             if (ep != nullptr) cp_async_8(c.sb + kOffRawSc + (rs * kRawBK + lane) * 8, sp);
             cp_async_arrive_noinc(full);  // one of the 32 async arrivals
-            const uint32_t maskA = __ballot_sync(0xffffffffu, vA && ep != nullptr);
-            const uint32_t maskB = p.pair ? __ballot_sync(0xffffffffu, vB && ep != nullptr) : maskA;
+            const uint32_t maskA = p.pair ? __ballot_sync(0xffffffffu, vA && ep != nullptr) : mask;
+            const uint32_t maskB = p.pair ? __ballot_sync(0xffffffffu, vB && ep != nullptr) : mask;
             if (lane == 0) {
                 st_shared_u32(c.sb + kOffRawMask + rs * 16, mask);
                 st_shared_u32(c.sb + kOffRawMask + rs * 16 + 4, maskA);
@@ -754,7 +754,7 @@ __device__ __forceinline__ float dequant_set(uint32_t raw, uint32_t rawsc, uint3
 // read the peer buffer), announced on XP_FULL so that QK(g) can start on those
 // dims; then the own set of raw tile 0 and 1 (once PV(g-2) has read the own
 // stage), each raw stage released after its own set; announced on X_FULL.
-__device__ void dequant_role(const Ctx& c, const UnitDesc* units, int n_units, int dw) {
+__device__ void dequant_role(const Ctx& c, const UnitDesc* units, int n_units, int dw, bool pair) {
     const int lane = threadIdx.x & 31;
     uint32_t g = 0;
     for (int ui = 0; ui < n_units; ++ui) {
@@ -775,8 +775,8 @@ __device__ void dequant_role(const Ctx& c, const UnitDesc* units, int n_units, i
                     const uint32_t m = ld_shared_u32(c.sb + kOffRawMask + rs * 16);
                     if (k == 0) mask0 = m; else mask1 = m;
                     if ((lane >> 1) == k && lane < 4) mab = ld_shared_u32(c.sb + kOffRawMask + rs * 16 + 4 + 4 * (lane & 1));
-                    mA[k] = ld_shared_u32(c.sb + kOffRawMask + rs * 16 + 4);
-                    mB[k] = ld_shared_u32(c.sb + kOffRawMask + rs * 16 + 8);
+                    mA[k] = pair ? ld_shared_u32(c.sb + kOffRawMask + rs * 16 + 4) : m;
+                    mB[k] = pair ? ld_shared_u32(c.sb + kOffRawMask + rs * 16 + 8) : m;
                     if (k == 0 && !wait_bar_warp(c, bar_addr(c, BAR_XP_EMPTY), (g & 1u) ^ 1u)) return;
                 } else if (k == 0) {
                     fence_proxy_async_smem();
@@ -798,8 +798,10 @@ __device__ void dequant_role(const Ctx& c, const UnitDesc* units, int n_units, i
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) vbound = fmaxf(vbound, __shfl_xor_sync(0xffffffffu, vbound, o));
             if (lane == 0) st_shared_f32(c.sb + kOffXVmax + (xs * kNumDequantWarps + dw) * 4, vbound);
-            poison = __reduce_or_sync(0xffffffffu, poison);
-            if (lane == 0) st_shared_u32(c.sb + kOffXPoison + (xs * kNumDequantWarps + dw) * 4, poison);
+            if (pair) {  // without pairing both rows are one: nothing is ever zeroed
+                poison = __reduce_or_sync(0xffffffffu, poison);
+                if (lane == 0) st_shared_u32(c.sb + kOffXPoison + (xs * kNumDequantWarps + dw) * 4, poison);
+            }
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive_local(bar_addr(c, BAR_X_FULL + xs));
@@ -1095,13 +1097,15 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, UnitDesc* units, in
             // sum.  Both sides take the same decision from the same values.
             const uint32_t vb = c.sb + kOffXVmax + xs * (4 * kNumDequantWarps);
             float vmax = ld_shared_f32(vb);
-            uint32_t pois = ld_shared_u32(c.sb + kOffXPoison + xs * (4 * kNumDequantWarps));
 #pragma unroll
-            for (int w = 1; w < kNumDequantWarps; ++w) {
-                vmax = fmaxf(vmax, ld_shared_f32(vb + 4 * w));
-                pois |= ld_shared_u32(c.sb + kOffXPoison + (xs * kNumDequantWarps + w) * 4);
+            for (int w = 1; w < kNumDequantWarps; ++w) vmax = fmaxf(vmax, ld_shared_f32(vb + 4 * w));
+            if (p.pair) {
+                uint32_t pois = 0u;
+#pragma unroll
+                for (int w = 0; w < kNumDequantWarps; ++w)
+                    pois |= ld_shared_u32(c.sb + kOffXPoison + (xs * kNumDequantWarps + w) * 4);
+                if (ok && ((pois >> sub) & 1u)) poisoned = true;
             }
-            if (ok && ((pois >> sub) & 1u)) poisoned = true;
             const float capk = 32.f * (1.0f / 512.0f) * (1.0f + 1.0f / 256.0f);
             const float cap0 = mt0 == -INFINITY ? 0.f : capk * ex2_approx(mt0 - msub);
             const float cap1 = mt1 == -INFINITY ? 0.f : capk * ex2_approx(mt1 - msub);
@@ -1625,7 +1629,7 @@ __global__ void __launch_bounds__(kThreads, 1) smla_decode_kernel(const KParams 
         if (lane == 0) mma_role(c, units, n_units);
         __syncwarp();
     } else {
-        dequant_role(c, units, n_units, warp - kDequantWarp0);
+        dequant_role(c, units, n_units, warp - kDequantWarp0, p.pair != 0);
     }
 
     tc_fence_before();
@@ -1674,11 +1678,13 @@ __global__ void __launch_bounds__(kMergeThreads) smla_merge_kernel(const KParams
     for (int j = 0; j < 8; ++j) acc[j] = 0.f;
 #pragma unroll 4
     for (int i = 0; i < sr; ++i) {
+        // O is loaded beside (m, l), so that the loads of successive partials
+        // overlap: every partial slot of the row was written by its unit
         const float2 mi = __ldcg(ml + i * ml_step);
-        lall += mi.y;
-        if (mi.x == -INFINITY) continue;  // saw no entry: its O is not read
         const float4 x0 = __ldcg(reinterpret_cast<const float4*>(po + i * po_step));
         const float4 x1 = __ldcg(reinterpret_cast<const float4*>(po + i * po_step) + 1);
+        lall += mi.y;
+        if (mi.x == -INFINITY) continue;  // saw no entry: its O is not used
         if (mi.x > M) {  // the running maximum grows: rescale what is summed so far
             const float f = M == -INFINITY ? 0.f : exp2f(M - mi.x);
             Z *= f;
