@@ -242,7 +242,8 @@ smla_status smla_cache_write(const void* latent, int64_t num_rows, const int64_t
  * Arguments (DEVICE pointers, caller-owned, 4-byte aligned): scores float32
  * [num_rows][stride]; lens int32 [num_rows]; out int32 [num_rows][k].
  * 1 <= k <= SMLA_TOPK_MAX_K, 0 <= stride < 2^31.  One kernel launch on
- * `stream` (one CTA per row); allocates nothing.
+ * `stream` (a cluster of two CTAs per row, each over half of it); allocates
+ * nothing.
  */
 smla_status smla_topk_indices(const float* scores, int64_t stride, const int32_t* lens, int32_t num_rows,
                               int32_t k, int32_t* out, smla_stream_t stream);

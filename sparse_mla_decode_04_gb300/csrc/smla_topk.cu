@@ -8,12 +8,24 @@
 // ascending; NaN scores are never selected; a row with fewer than k
 // selectable positions is padded with -1.
 //
-// One CTA per row.  Scores map to order-preserving 32-bit keys (NaN -> 0, the
-// one key never selected).  A radix select over the key's 11 + 11 + 10 bits
-// (histograms in shared memory) finds the k-th largest key T; one more pass
-// collects every key above T and, in position order, the first positions
-// equal to T; a bitonic sort in shared memory orders the k results.
+// A cluster of two CTAs per row, each over a contiguous half of it; their
+// histograms are summed through distributed shared memory and every selected
+// key lands in the first CTA's buffer.  Scores map to order-preserving 32-bit
+// keys (NaN -> 0, the one key never selected).  A radix select over the key's
+// 13 + 11 + 8 bits (histograms in shared memory; the bin holding the k-th
+// largest key found by a block-wide suffix scan) narrows the k-th largest key
+// down.  As soon as the keys at or above the current bin number at most
+// SMLA_TOPK_MAX_K (after any pass, or at once when the row holds that few valid
+// keys), one more pass over the row collects exactly those keys, and a bitonic
+// sort in shared memory (key descending, position ascending) puts the k
+// selected first.  Otherwise (many keys tied at the threshold) the third pass
+// gives the k-th largest key T, and a collecting pass takes every key above T
+// and, in position order (the second half's ties after the first's), the first
+// positions equal to T, then sorts them.
+#include <atomic>
 #include <cstdint>
+#include <mutex>
+#include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
 #include "smla.h"
@@ -22,8 +34,13 @@
 namespace smla {
 namespace {
 
+namespace cg = cooperative_groups;
+
 constexpr int kThreadsTopk = 1024;
 constexpr int kMaxK = SMLA_TOPK_MAX_K;
+constexpr int kMaxBins = 1 << 13;  // the first pass's histogram
+constexpr int kCluster = 2;        // CTAs per row (a thread-block cluster), each over a contiguous part
+constexpr size_t kTopkSmem = kMaxK * 8 + 2 * kMaxBins * 4;  // selection + part and cluster histograms
 
 // Order-preserving key: a larger score gives a larger key; -0 and +0 are one
 // key (they compare equal); NaN gives 0, the one key never selected.
@@ -33,84 +50,170 @@ __device__ __forceinline__ uint32_t sort_key(float f) {
     return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
-__global__ void __launch_bounds__(kThreadsTopk) smla_topk_kernel(const float* __restrict__ scores, int64_t stride,
-                                                                 const int32_t* __restrict__ lens, int k,
-                                                                 int32_t* __restrict__ out) {
-    __shared__ uint32_t hist[2048];
-    __shared__ unsigned long long sel[kMaxK];  // (key << 32) | ~position: larger = earlier in the output
-    __shared__ uint32_t s_prefix, s_mask, s_need, s_count, s_gt;
+// Calls f(score, position) for every position of [0, L) of `row`: 16-byte
+// loads where the row is 16-byte aligned, four of them in flight per thread.
+template <class F>
+__device__ __forceinline__ void for_each_score(const float* __restrict__ row, int L, bool vec4, F f) {
+    const int tid = threadIdx.x;
+    if (vec4) {
+        const float4* row4 = reinterpret_cast<const float4*>(row);
+        const int n4 = L / 4;
+        int i = tid;
+        for (; i + 3 * kThreadsTopk < n4; i += 4 * kThreadsTopk) {
+            float4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) v[u] = __ldg(row4 + i + u * kThreadsTopk);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int b = 4 * (i + u * kThreadsTopk);
+                f(v[u].x, b); f(v[u].y, b + 1); f(v[u].z, b + 2); f(v[u].w, b + 3);
+            }
+        }
+        for (; i < n4; i += kThreadsTopk) {
+            const float4 v = __ldg(row4 + i);
+            f(v.x, 4 * i); f(v.y, 4 * i + 1); f(v.z, 4 * i + 2); f(v.w, 4 * i + 3);
+        }
+        for (int j = (L & ~3) + tid; j < L; j += kThreadsTopk) f(__ldg(row + j), j);
+    } else {
+        for (int j = tid; j < L; j += kThreadsTopk) f(__ldg(row + j), j);
+    }
+}
+
+// The bin b of hist[0, nb) holding the need-th largest key (need >= 1): the
+// largest b with sum_{j >= b} hist[j] >= need, and acc = sum_{j > b} hist[j];
+// b = 0 when the bins hold fewer than need keys.  Thread t sums bins
+// [t per, (t + 1) per); a block suffix scan of those sums points one thread at
+// the crossing, which walks its own bins.  Written by that thread into *b_out
+// and *acc_out; the total into *tot_out (thread 0) unless it is null.  All
+// threads call it.
+__device__ __forceinline__ void find_bin(const uint32_t* hist, int nb, uint32_t need, uint32_t* s_warp,
+                                         uint32_t* b_out, uint32_t* acc_out, uint32_t* tot_out) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int per = max(1, nb / kThreadsTopk);
+    const int lo = tid * per, hi = min(nb, lo + per);
+    uint32_t sum = 0;
+    for (int b = lo; b < hi; ++b) sum += hist[b];
+    // inclusive suffix sum over the warp's lanes (lanes above this one, and it)
+    uint32_t suf = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t v = __shfl_down_sync(0xffffffffu, suf, o);
+        if (lane + o < 32) suf += v;
+    }
+    if (lane == 0) s_warp[warp] = suf;  // the warp's total
+    __syncthreads();
+    uint32_t above = suf - sum;  // lanes above in this warp
+    for (int w = warp + 1; w < kThreadsTopk / 32; ++w) above += s_warp[w];
+    const uint32_t total_here = above + sum;
+    const bool mine = (above < need && need <= total_here) || (tid == 0 && total_here < need);
+    if (mine) {
+        uint32_t acc = above;
+        int b = hi - 1;
+        for (; b > lo; --b) {
+            if (acc + hist[b] >= need) break;
+            acc += hist[b];
+        }
+        *b_out = (uint32_t)b;
+        *acc_out = acc;
+    }
+    if (tid == 0 && tot_out != nullptr) *tot_out = total_here;
+    __syncthreads();
+}
+
+__device__ __forceinline__ unsigned long long sel_item(uint32_t key, int pos) {
+    return ((unsigned long long)key << 32) | (uint32_t)~(uint32_t)pos;  // larger = earlier in the output
+}
+
+__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreadsTopk)
+    smla_topk_kernel(const float* __restrict__ scores, int64_t stride, const int32_t* __restrict__ lens, int k,
+                     int32_t* __restrict__ out) {
+    extern __shared__ unsigned long long topk_smem[];
+    unsigned long long* sel = topk_smem;                                         // [kMaxK] (rank 0 gathers)
+    uint32_t* hist = reinterpret_cast<uint32_t*>(topk_smem + kMaxK);              // [kMaxBins] this CTA's part
+    uint32_t* comb = hist + kMaxBins;                                             // [kMaxBins] the cluster's sum
+    __shared__ uint32_t s_prefix, s_mask, s_need, s_count, s_total, s_bin, s_b, s_acc;
     __shared__ uint32_t s_warp[kThreadsTopk / 32];
-    const int r = blockIdx.x, tid = threadIdx.x;
+    cg::cluster_group cl = cg::this_cluster();
+    const int rank = (int)cl.block_rank();
+    const int r = blockIdx.x / kCluster, tid = threadIdx.x;
     const float* row = scores + (int64_t)r * stride;
     const int L = (int)min((int64_t)max(0, __ldg(lens + r)), stride);  // lengths past the row's capacity are cut
     const bool vec4 = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;    // 16-byte loads where the row allows
-    // ---- radix select: the k-th largest key among keys >= 1
-    if (tid == 0) { s_prefix = 0u; s_mask = 0u; s_need = (uint32_t)k; }
-    const int shifts[3] = {21, 10, 0};
-    const int widths[3] = {11, 11, 10};
-    uint32_t total_valid = 0;
+    // this CTA's contiguous part of the row (a multiple of 4 positions long)
+    const int seg = ((L + kCluster - 1) / kCluster + 3) & ~3;
+    const int beg = min(L, rank * seg), end = min(L, beg + seg);
+    const float* part = row + beg;
+    // rank 0's counter and selection buffer, which every CTA of the cluster fills
+    uint32_t* cnt0 = cl.map_shared_rank(&s_count, 0);
+    unsigned long long* sel0 = cl.map_shared_rank(sel, 0);
+    if (tid == 0) { s_prefix = 0u; s_mask = 0u; s_need = (uint32_t)k; s_count = 0u; }
+    const int shifts[3] = {19, 8, 0};
+    const int widths[3] = {13, 11, 8};
+    bool fast = false;
 #pragma unroll 1
     for (int pass = 0; pass < 3; ++pass) {
         const int sh = shifts[pass], nb = 1 << widths[pass];
         for (int i = tid; i < nb; i += kThreadsTopk) hist[i] = 0u;
         __syncthreads();
         const uint32_t prefix = s_prefix, mask = s_mask;
-        auto count = [&](float f) {
+        for_each_score(part, end - beg, vec4, [&](float f, int) {
             const uint32_t key = sort_key(f);
             if (key != 0u && (key & mask) == prefix) atomicAdd(&hist[(key >> sh) & (uint32_t)(nb - 1)], 1u);
-        };
-        if (vec4) {
-            const float4* row4 = reinterpret_cast<const float4*>(row);
-            for (int i = tid; i < L / 4; i += kThreadsTopk) {
-                const float4 v = __ldg(row4 + i);
-                count(v.x); count(v.y); count(v.z); count(v.w);
-            }
-            for (int i = (L & ~3) + tid; i < L; i += kThreadsTopk) count(__ldg(row + i));
-        } else {
-            for (int i = tid; i < L; i += kThreadsTopk) count(__ldg(row + i));
+        });
+        cl.sync();  // every part's histogram is complete (and rank 0's counter is zero)
+        for (int i = tid; i < nb; i += kThreadsTopk) {
+            uint32_t v = 0;
+#pragma unroll
+            for (int q = 0; q < kCluster; ++q) v += cl.map_shared_rank(hist, q)[i];
+            comb[i] = v;
         }
         __syncthreads();
-        if (tid == 0) {  // walk the bins from the top until the k-th key's bin
-            uint32_t need = s_need, acc = 0;
-            int b = nb - 1;
-            if (pass == 0) {
-                uint32_t tot = 0;
-                for (int j = 0; j < nb; ++j) tot += hist[j];
-                s_count = tot;  // valid keys in the row
-            }
-            for (; b > 0; --b) {
-                if (acc + hist[b] >= need) break;
-                acc += hist[b];
-            }
-            s_need = need - acc;  // still needed from bin b
-            s_prefix = prefix | ((uint32_t)b << sh);
+        const uint32_t need = s_need;
+        find_bin(comb, nb, need, s_warp, &s_b, &s_acc, pass == 0 ? &s_total : nullptr);
+        if (tid == 0) {
+            const uint32_t b = s_b;
+            s_need = need - s_acc;  // still needed from bin b
+            s_bin = comb[b];
+            s_prefix = prefix | (b << sh);
             s_mask = mask | ((uint32_t)(nb - 1) << sh);
         }
         __syncthreads();
-        if (pass == 0) total_valid = s_count;
-    }
-    // T = s_prefix; every key > T is taken, and s_need keys equal to T (the
-    // smallest positions).  With fewer valid keys than k, take them all.
-    const bool take_all = total_valid <= (uint32_t)k;
-    const uint32_t T = take_all ? 1u : s_prefix;
-    const uint32_t need_eq = take_all ? 0xFFFFFFFFu : s_need;
-    const int n_sel = take_all ? (int)total_valid : k;
-    if (tid == 0) { s_count = 0u; s_gt = 0u; }
-    __syncthreads();
-    // ---- collect: keys above T anywhere; keys equal to T in position order
-    uint32_t eq_base = 0;  // equal keys taken by earlier chunks
-    for (int base = 0; base < L; base += kThreadsTopk) {
-        const int i = base + tid;
-        const uint32_t key = i < L ? sort_key(__ldg(row + i)) : 0u;
-        const unsigned long long item = ((unsigned long long)key << 32) | (uint32_t)~(uint32_t)i;
-        if (key > T || (take_all && key != 0u)) {
-            const uint32_t slot = atomicAdd(&s_count, 1u);
-            sel[slot] = item;
+        // keys at or above the bin: k - need above it, plus the bin's own
+        const uint32_t at_or_above = (uint32_t)k - s_need + s_bin;
+        const bool all_fit = pass == 0 && s_total <= (uint32_t)kMaxK;
+        if (all_fit || at_or_above <= (uint32_t)kMaxK) {
+            // one pass collects them, unordered, into rank 0's buffer
+            const uint32_t cp = all_fit ? 0u : s_prefix, cm = all_fit ? 0u : s_mask;
+            for_each_score(part, end - beg, vec4, [&](float f, int i) {
+                const uint32_t key = sort_key(f);
+                if (key != 0u && (key & cm) >= cp) {
+                    const uint32_t slot = atomicAdd(cnt0, 1u);
+                    if (slot < (uint32_t)kMaxK) sel0[slot] = sel_item(key, beg + i);
+                }
+            });
+            fast = true;
+            break;
         }
-        if (!take_all) {  // equal keys: taken in position order until need_eq
+        if (pass < 2) cl.sync();  // the other parts have read this histogram before it is cleared
+    }
+    if (!fast) {
+        // Many keys tied at the threshold: T = s_prefix is the k-th largest key;
+        // every key > T is taken, and s_need keys equal to T (the smallest
+        // positions), collected in position order: this part's ties follow
+        // those of the parts before it, counted by their last histograms.
+        const uint32_t T = s_prefix, need_eq = s_need, bT = T & 0xFFu;
+        uint32_t eq_base = 0;  // equal keys taken before this part's current chunk
+        for (int q = 0; q < rank; ++q) eq_base += cl.map_shared_rank(hist, q)[bT];
+        for (int base = beg; base < end; base += kThreadsTopk) {
+            const int i = base + tid;
+            const uint32_t key = i < end ? sort_key(__ldg(row + i)) : 0u;
+            if (key > T) {
+                const uint32_t slot = atomicAdd(cnt0, 1u);
+                sel0[slot] = sel_item(key, i);
+            }
             const bool eq = key == T && key != 0u;
             const uint32_t chunk_total = (uint32_t)__syncthreads_count(eq);
-            if (chunk_total != 0u && eq_base < need_eq) {  // block-uniform: the rare chunks holding T
+            if (chunk_total != 0u && eq_base < need_eq) {  // block-uniform: the chunks holding T
                 const uint32_t ballot = __ballot_sync(0xffffffffu, eq);
                 if ((tid & 31) == 0) s_warp[tid >> 5] = __popc(ballot);
                 __syncthreads();
@@ -118,16 +221,18 @@ __global__ void __launch_bounds__(kThreadsTopk) smla_topk_kernel(const float* __
                 for (int w = 0; w < (tid >> 5); ++w) before += s_warp[w];
                 before += __popc(ballot & ((1u << (tid & 31)) - 1u));
                 if (eq && before < need_eq) {
-                    const uint32_t slot = atomicAdd(&s_count, 1u);
-                    sel[slot] = item;
+                    const uint32_t slot = atomicAdd(cnt0, 1u);
+                    sel0[slot] = sel_item(key, i);
                 }
                 __syncthreads();
             }
             eq_base += chunk_total;
         }
     }
-    __syncthreads();
-    // ---- bitonic sort of the selected items, descending (pad with 0)
+    cl.sync();  // every part's keys sit in rank 0's buffer; no CTA reads another's memory after this
+    if (rank != 0) return;
+    const int n_sel = fast ? (int)min(s_count, (uint32_t)kMaxK) : k;
+    // ---- bitonic sort of the n_sel items, descending (padded with 0)
     int n2 = 1;
     while (n2 < n_sel) n2 <<= 1;
     for (int i = n_sel + tid; i < n2; i += kThreadsTopk) sel[i] = 0ull;
@@ -145,8 +250,27 @@ __global__ void __launch_bounds__(kThreadsTopk) smla_topk_kernel(const float* __
             __syncthreads();
         }
     }
+    const int n_out = min(n_sel, k);
     for (int i = tid; i < k; i += kThreadsTopk)
-        out[(int64_t)r * k + i] = i < n_sel ? (int32_t)~(uint32_t)(sel[i] & 0xFFFFFFFFull) : -1;
+        out[(int64_t)r * k + i] = i < n_out ? (int32_t)~(uint32_t)(sel[i] & 0xFFFFFFFFull) : -1;
+}
+
+std::atomic<int> g_topk_attr[64];
+std::mutex g_topk_mu;
+
+// The kernel takes more than 48 KB of dynamic shared memory: opt in once per device.
+cudaError_t ensure_topk_attrs() {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (g_topk_attr[dev].load(std::memory_order_acquire) == 1) return cudaSuccess;
+    std::lock_guard<std::mutex> lk(g_topk_mu);
+    if (g_topk_attr[dev].load(std::memory_order_relaxed) == 1) return cudaSuccess;
+    e = cudaFuncSetAttribute(smla_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTopkSmem);
+    if (e != cudaSuccess) return e;
+    g_topk_attr[dev].store(1, std::memory_order_release);
+    return cudaSuccess;
 }
 
 }  // namespace
@@ -163,6 +287,8 @@ extern "C" smla_status smla_topk_indices(const float* scores, int64_t stride, co
         return SMLA_ERR_MISALIGNED;
     const smla_status dev = check_device_only();
     if (dev != SMLA_OK) return dev;
-    smla_topk_kernel<<<num_rows, kThreadsTopk, 0, static_cast<cudaStream_t>(stream)>>>(scores, stride, lens, k, out);
+    if (ensure_topk_attrs() != cudaSuccess) return SMLA_ERR_CUDA;
+    smla_topk_kernel<<<num_rows * kCluster, kThreadsTopk, kTopkSmem, static_cast<cudaStream_t>(stream)>>>(scores, stride, lens, k,
+                                                                                                out);
     return cudaGetLastError() == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA;
 }

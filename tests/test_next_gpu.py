@@ -127,3 +127,17 @@ def test_topk_full_size_sampled_rows(cuda_device):
     for r in (0, 1, 63):
         ref = O.topk_indices(s[r:r + 1].cpu().numpy(), [int(lens[r])], 2048)
         assert np.array_equal(got[r:r + 1].cpu().numpy(), ref)
+
+
+def test_topk_many_ties_at_the_threshold(cuda_device):
+    """More keys tied at the k-th score than the selection buffer holds: the
+    ordered collection takes the smallest positions among the ties."""
+    R, L = 3, 30000
+    s = torch.zeros((R, L))
+    s[0, ::7] = 1.0                      # 4286 ones, then 25714 zeros tied for the rest
+    s[1, :] = 2.5                        # every score equal
+    s[2, 5000:] = torch.randn(L - 5000, generator=torch.Generator().manual_seed(3)).round()  # integer ties
+    lens = torch.full((R,), L, dtype=torch.int32)
+    for k in (100, 4096):
+        got = smla.topk_indices(s.cuda(), lens.cuda(), k).cpu().numpy()
+        assert np.array_equal(got, O.topk_indices(s.numpy(), lens.numpy(), k))
