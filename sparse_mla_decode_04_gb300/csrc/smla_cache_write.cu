@@ -15,8 +15,10 @@
 // The path is HBM-bound: 1024 bytes read and 584 written per row.
 #include <algorithm>
 #include <cstdint>
-#include <cuda_runtime.h>
+#include <cstring>
+#include <cuda_bf16.h>
 #include <cuda_fp8.h>
+#include <cuda_runtime.h>
 
 #include "smla.h"
 #include "smla_internal.h"
@@ -25,6 +27,7 @@ namespace smla {
 namespace {
 
 constexpr int kWarpsPerBlock = 8;
+constexpr int kRowsInFlight = 2;  // rows a warp loads before converting any
 
 // Smallest code c in [0, 254] with amax <= 448 * 2^(c - 127), from the fp32
 // bits of amax (>= 0, not NaN): amax = m 2^e, 448 = 1.75 2^8, so
@@ -43,15 +46,19 @@ __device__ __forceinline__ float inv_scale(uint32_t code) {
     return code <= 253u ? __uint_as_float((254u - code) << 23) : __uint_as_float(0x00400000u);
 }
 
-// Two values -> two e4m3 bytes (low byte = a).
-__device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
-    uint32_t r = (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
-    uint32_t lo = r & 0xFFu, hi = r >> 8;
-    if (a != a) lo = 0x7Fu;
-    else if ((lo & 0x7Fu) == 0u) lo = 0u;
-    if (b != b) hi = 0x7Fu;
-    else if ((hi & 0x7Fu) == 0u) hi = 0u;
-    return lo | (hi << 8);
+// Four values -> four e4m3 bytes (lowest byte = a).  The conversion rounds to
+// nearest even and saturates finite values at +-448 (0x7E); a NaN comes out
+// with magnitude 0x7F and loses its sign here, and a zero of either sign
+// becomes 0x00, four bytes at a time: for a magnitude m <= 0x7F, bit 7 of
+// m + 0x7F is set iff m != 0 and bit 7 of m + 1 iff m == 0x7F (no carry leaves
+// a byte).
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
+    const uint32_t r = (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3) |
+                       ((uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3) << 16);
+    const uint32_t mag = r & 0x7F7F7F7Fu;
+    const uint32_t nonzero = (mag + 0x7F7F7F7Fu) & 0x80808080u;
+    const uint32_t nan = (mag + 0x01010101u) & 0x80808080u;
+    return r & ((nonzero >> 7) * 0xFFu) & ~nan;
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -64,6 +71,53 @@ __device__ __forceinline__ uint32_t canon_nan_bf16x2(uint32_t w) {
     return lo | (hi << 16);
 }
 
+// One row: w holds this lane's 16 dims (dims 16 lane .. 16 lane + 15).
+__device__ __forceinline__ void write_row(const uint32_t (&w)[8], int lane, uint8_t* dst, uint8_t* sdst) {
+    // every lane takes part in the group reductions (shuffles); RoPE lanes
+    // contribute a dummy zero that never leaves their own 4-lane group
+    // |x| maxima on bf16 pairs (a NaN is passed over, as fmaxf does)
+    __nv_bfloat162 m2 = __float2bfloat162_rn(0.f);
+    if (lane < 28) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t a = w[i] & 0x7FFF7FFFu;
+            __nv_bfloat162 v;
+            memcpy(&v, &a, 4);
+            m2 = __hmax2(m2, v);
+        }
+    }
+    float amax = fmaxf(__low2float(m2), __high2float(m2));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    const uint32_t code = ue8m0_code(amax);
+    if (lane < 28) {
+        const float f = inv_scale(code);
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            o[i] = e4m3x4(bf16_lo(w[2 * i]) * f, bf16_hi(w[2 * i]) * f, bf16_lo(w[2 * i + 1]) * f,
+                          bf16_hi(w[2 * i + 1]) * f);
+        __stcs(reinterpret_cast<uint4*>(dst + 16 * lane), make_uint4(o[0], o[1], o[2], o[3]));
+    } else {
+        uint4 r0, r1;
+        r0.x = canon_nan_bf16x2(w[0]); r0.y = canon_nan_bf16x2(w[1]);
+        r0.z = canon_nan_bf16x2(w[2]); r0.w = canon_nan_bf16x2(w[3]);
+        r1.x = canon_nan_bf16x2(w[4]); r1.y = canon_nan_bf16x2(w[5]);
+        r1.z = canon_nan_bf16x2(w[6]); r1.w = canon_nan_bf16x2(w[7]);
+        uint4* rd = reinterpret_cast<uint4*>(dst + SMLA_NOPE_DIMS + 32 * (lane - 28));
+        __stcs(rd, r0);
+        __stcs(rd + 1, r1);
+    }
+    // the 7 codes (lanes 0, 4, ..., 24) and a zero pad byte, one 8-byte store
+    uint32_t lo = 0, hi = 0;
+#pragma unroll
+    for (int g = 0; g < 7; ++g) {
+        const uint32_t cg = __shfl_sync(0xffffffffu, code, 4 * g);
+        if (g < 4) lo |= cg << (8 * g); else hi |= cg << (8 * (g - 4));
+    }
+    if (lane == 0) *reinterpret_cast<uint2*>(sdst) = make_uint2(lo, hi);
+}
+
 __global__ void __launch_bounds__(32 * kWarpsPerBlock) smla_cache_write_kernel(
     const uint4* __restrict__ latent, int64_t num_rows, const int64_t* __restrict__ slots, uint8_t* __restrict__ pool,
     uint8_t* __restrict__ scales, int64_t n_pool, uint32_t* err) {
@@ -71,55 +125,32 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock) smla_cache_write_kernel(
     const int64_t warp0 = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
     const int64_t nwarps = (int64_t)gridDim.x * kWarpsPerBlock;
     uint32_t bad = 0;
-    for (int64_t row = warp0; row < num_rows; row += nwarps) {
-        const int64_t s = __ldg(slots + row);
-        if (s == -1) continue;
-        if (s < -1 || s >= n_pool) {
-            bad = 1;
-            continue;
-        }
-        const uint4 v0 = __ldg(latent + row * 64 + 2 * lane);      // dims 16 l .. 16 l + 7
-        const uint4 v1 = __ldg(latent + row * 64 + 2 * lane + 1);  // dims 16 l + 8 .. 16 l + 15
-        const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-        uint8_t* dst = pool + s * SMLA_ENTRY_BYTES;
-        // every lane takes part in the group reductions (shuffles); RoPE lanes
-        // contribute a dummy zero that never leaves their own 4-lane group
-        float amax = 0.f;
-        if (lane < 28) {
+    // kRowsInFlight rows per warp step, all their loads issued before any is used
+    for (int64_t row0 = warp0; row0 < num_rows; row0 += kRowsInFlight * nwarps) {
+        uint32_t w[kRowsInFlight][8];
+        int64_t sl[kRowsInFlight];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
-        }
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-        const uint32_t code = ue8m0_code(amax);
-        if (lane < 28) {
-            const float f = inv_scale(code);
-            uint32_t o[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint32_t p0 = e4m3x2(bf16_lo(w[2 * i]) * f, bf16_hi(w[2 * i]) * f);
-                const uint32_t p1 = e4m3x2(bf16_lo(w[2 * i + 1]) * f, bf16_hi(w[2 * i + 1]) * f);
-                o[i] = p0 | (p1 << 16);
+        for (int u = 0; u < kRowsInFlight; ++u) {
+            const int64_t row = row0 + u * nwarps;
+            sl[u] = -1;
+            if (row < num_rows) {
+                sl[u] = __ldcs(slots + row);
+                const uint4 v0 = __ldcs(latent + row * 64 + 2 * lane);      // dims 16 l .. 16 l + 7
+                const uint4 v1 = __ldcs(latent + row * 64 + 2 * lane + 1);  // dims 16 l + 8 .. 16 l + 15
+                w[u][0] = v0.x; w[u][1] = v0.y; w[u][2] = v0.z; w[u][3] = v0.w;
+                w[u][4] = v1.x; w[u][5] = v1.y; w[u][6] = v1.z; w[u][7] = v1.w;
             }
-            *reinterpret_cast<uint4*>(dst + 16 * lane) = make_uint4(o[0], o[1], o[2], o[3]);
-        } else {
-            uint4 r0, r1;
-            r0.x = canon_nan_bf16x2(w[0]); r0.y = canon_nan_bf16x2(w[1]);
-            r0.z = canon_nan_bf16x2(w[2]); r0.w = canon_nan_bf16x2(w[3]);
-            r1.x = canon_nan_bf16x2(w[4]); r1.y = canon_nan_bf16x2(w[5]);
-            r1.z = canon_nan_bf16x2(w[6]); r1.w = canon_nan_bf16x2(w[7]);
-            uint4* rd = reinterpret_cast<uint4*>(dst + SMLA_NOPE_DIMS + 32 * (lane - 28));
-            rd[0] = r0;
-            rd[1] = r1;
         }
-        // the 7 codes (lanes 0, 4, ..., 24) and a zero pad byte, one 8-byte store
-        uint32_t lo = 0, hi = 0;
 #pragma unroll
-        for (int g = 0; g < 7; ++g) {
-            const uint32_t cg = __shfl_sync(0xffffffffu, code, 4 * g);
-            if (g < 4) lo |= cg << (8 * g); else hi |= cg << (8 * (g - 4));
+        for (int u = 0; u < kRowsInFlight; ++u) {
+            const int64_t s = sl[u];  // -1 also for rows past the end
+            if (s == -1) continue;    // warp-uniform
+            if (s < -1 || s >= n_pool) {
+                bad = 1;
+                continue;
+            }
+            write_row(w[u], lane, pool + s * SMLA_ENTRY_BYTES, scales + s * SMLA_SCALE_BYTES);
         }
-        if (lane == 0) *reinterpret_cast<uint2*>(scales + s * SMLA_SCALE_BYTES) = make_uint2(lo, hi);
     }
     if (err != nullptr && __any_sync(0xffffffffu, bad != 0) && lane == 0) atomicOr(err, SMLA_DEV_BAD_INDEX);
 }
@@ -140,11 +171,14 @@ extern "C" smla_status smla_cache_write(const void* latent, int64_t num_rows, co
         return SMLA_ERR_MISALIGNED;
     const smla_status dev = check_device_only();
     if (dev != SMLA_OK) return dev;
-    int sms = 0, d = 0;
-    if (cudaGetDevice(&d) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, d) != cudaSuccess)
+    int sms = 0, d = 0, per_sm = 0;
+    if (cudaGetDevice(&d) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, d) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, smla_cache_write_kernel, 32 * kWarpsPerBlock, 0) !=
+            cudaSuccess)
         return SMLA_ERR_CUDA;
+    // one resident wave of blocks, each warp striding over the rows
     const int64_t blocks_needed = (num_rows + kWarpsPerBlock - 1) / kWarpsPerBlock;
-    const int blocks = (int)std::min<int64_t>(blocks_needed, (int64_t)sms * 8);
+    const int blocks = (int)std::min<int64_t>(blocks_needed, (int64_t)sms * std::max(1, per_sm));
     smla_cache_write_kernel<<<blocks, 32 * kWarpsPerBlock, 0, static_cast<cudaStream_t>(stream)>>>(
         static_cast<const uint4*>(latent), num_rows, slots, static_cast<uint8_t*>(pool), static_cast<uint8_t*>(scales),
         n_pool, dev_error);
