@@ -366,7 +366,8 @@ def per_config_lines(names, dev, flush_buf, stream, peaks, steps: int, warmup: i
     return res
 
 
-def next_rows_lines(dev, flush_buf, stream, peaks, steps: int, warmup: int = 3):
+def next_rows_lines(dev, flush_buf, stream, peaks, steps: int, warmup: int = 3, writer_rows: int = 4 << 20,
+                    topk_rows: int = 64):
     """The two producers beside the decode, each timed alone (CUDA events on
     the launching stream, L2 flushed before each step), against the HBM
     roofline of their algorithmic bytes:
@@ -398,7 +399,7 @@ def next_rows_lines(dev, flush_buf, stream, peaks, steps: int, warmup: int = 3):
 
     g = torch.Generator(device=dev)
     g.manual_seed(77)
-    n = 4 << 20
+    n = writer_rows
     lat = (torch.randn((n, 512), generator=g, device=dev)).to(torch.bfloat16)
     slots = torch.randperm(n, generator=g, device=dev)
     pool = torch.empty((n, 576), dtype=torch.uint8, device=dev)
@@ -413,7 +414,7 @@ def next_rows_lines(dev, flush_buf, stream, peaks, steps: int, warmup: int = 3):
     del lat, slots, pool, sc
     gc.collect()
     torch.cuda.empty_cache()
-    R, L, k = 64, 1 << 20, 2048
+    R, L, k = topk_rows, 1 << 20, 2048
     scores = torch.randn((R, L), generator=g, device=dev)
     lens = torch.full((R,), L, dtype=torch.int32, device=dev)
     out = torch.empty((R, k), dtype=torch.int32, device=dev)
@@ -443,6 +444,14 @@ def run_gpu(args):
     import sparse_mla_decode_04_gb300 as smla
 
     smla.build()
+    if args.next_only:  # the two producers alone, one JSON object (not a bench line)
+        if rank == 0:
+            fb = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+            peaks, _ = load_peaks()
+            res = next_rows_lines(dev, fb, torch.cuda.Stream(device=dev), peaks, args.config_steps,
+                                  writer_rows=args.next_writer_rows, topk_rows=args.next_topk_rows)
+            print(json.dumps({"next_rows": res}), flush=True)
+        return 0
     p = make_workload(args.workload, dev)
     if rank > 0:  # replicas draw different data
         p.q_nope.copy_(torch.randn_like(p.q_nope, dtype=torch.float32).to(torch.bfloat16))
@@ -556,7 +565,8 @@ def run_gpu(args):
     if rank == 0 and world == 1 and not args.no_per_config:
         names = [n for n in PER_CONFIG if n != args.workload]
         line["per_config"] = per_config_lines(names, dev, flush_buf, stream, peaks, args.config_steps, 3)
-        line["next_rows"] = next_rows_lines(dev, flush_buf, stream, peaks, args.config_steps)
+        line["next_rows"] = next_rows_lines(dev, flush_buf, stream, peaks, args.config_steps,
+                                            writer_rows=args.next_writer_rows, topk_rows=args.next_topk_rows)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -576,6 +586,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", action="store_true", help="time only the main workload")
     ap.add_argument("--config-steps", type=int, default=10, help="timed steps per per_config workload")
+    ap.add_argument("--next-only", action="store_true",
+                    help="time only the cache writer and the top-k producer (for profiling them)")
+    ap.add_argument("--next-writer-rows", type=int, default=4 << 20, help="latent rows of the cache-writer line")
+    ap.add_argument("--next-topk-rows", type=int, default=64, help="score rows (1M each) of the top-k line")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
