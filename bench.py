@@ -102,17 +102,20 @@ def load_peaks():
 
 
 def kernel_source_hash():
-    """Hash of the device sources' code: comments and whitespace are left out,
-    so that only a change to the compiled kernel makes recorded counters stale."""
+    """Hash of the decode kernel's sources (its translation unit and the
+    headers it includes): comments and whitespace are left out, so that only
+    a change to the compiled kernel makes recorded counters stale."""
     h = hashlib.sha256()
-    for fn in sorted(os.listdir(os.path.dirname(KERNEL_SRC))):
-        if fn.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(os.path.dirname(KERNEL_SRC), fn)) as f:
-                src = f.read()
-            src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
-            src = re.sub(r"//[^\n]*", " ", src)
-            h.update(fn.encode())
-            h.update(" ".join(src.split()).encode())
+    csrc = os.path.dirname(KERNEL_SRC)
+    files = [os.path.join(csrc, "smla_decode.cu"), os.path.join(csrc, "sm103_ptx.cuh"),
+             os.path.join(csrc, "smla_internal.h"), os.path.join(ROOT, "include", "smla.h")]
+    for path in files:
+        with open(path) as f:
+            src = f.read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", " ", src)
+        h.update(os.path.basename(path).encode())
+        h.update(" ".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 
