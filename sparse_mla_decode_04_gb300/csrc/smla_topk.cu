@@ -11,17 +11,22 @@
 // A cluster of two CTAs per row, each over a contiguous half of it; their
 // histograms are summed through distributed shared memory and every selected
 // key lands in the first CTA's buffer.  Scores map to order-preserving 32-bit
-// keys (NaN -> 0, the one key never selected).  A radix select over the key's
-// 13 + 11 + 8 bits (histograms in shared memory; the bin holding the k-th
-// largest key found by a block-wide suffix scan) narrows the k-th largest key
-// down.  As soon as the keys at or above the current bin number at most
-// SMLA_TOPK_MAX_K (after any pass, or at once when the row holds that few valid
-// keys), one more pass over the row collects exactly those keys, and a bitonic
-// sort in shared memory (key descending, position ascending) puts the k
-// selected first.  Otherwise (many keys tied at the threshold) the third pass
-// gives the k-th largest key T, and a collecting pass takes every key above T
-// and, in position order (the second half's ties after the first's), the first
-// positions equal to T, then sorts them.
+// keys (NaN -> 0, the one key never selected).
+//
+// Usually one read of the row: a sample (the first 64 scores of every 1024)
+// places a 24-bit key prefix tau that about 1.45 k keys reach; the first pass
+// counts the 13-bit histogram of the row and collects every key whose prefix
+// is >= tau.  When that collected between k (or every valid key) and
+// SMLA_TOPK_MAX_K keys, they hold the top k: the pass ends there.  Otherwise
+// the radix select goes on (13 + 11 + 8 key bits, the bin of the k-th largest
+// key found by a block-wide suffix scan): as soon as the keys at or above the
+// current bin number at most SMLA_TOPK_MAX_K, one more pass collects exactly
+// those; with many keys tied at the threshold, the third pass gives the k-th
+// largest key T and a collecting pass takes every key above T and, in
+// position order (the second half's ties after the first's), the first
+// positions equal to T.  The collected keys are sorted in shared memory (key
+// descending, position ascending): each warp sorts 128 in registers, then
+// merge-path merges join the sorted lists.
 #include <atomic>
 #include <cstdint>
 #include <mutex>
@@ -39,6 +44,7 @@ namespace cg = cooperative_groups;
 constexpr int kThreadsTopk = 1024;
 constexpr int kMaxK = SMLA_TOPK_MAX_K;
 constexpr int kMaxBins = 1 << 13;  // the first pass's histogram
+constexpr int kGuessNum = 29, kGuessDen = 20;  // kGuessFactor = 1.45: the guess aims at 1.45 k keys
 constexpr int kCluster = 2;        // CTAs per row (a thread-block cluster), each over a contiguous part
 constexpr size_t kTopkSmem = kMaxK * 8 + 2 * kMaxBins * 4;  // selection + part and cluster histograms
 
@@ -131,7 +137,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreadsTopk)
     unsigned long long* sel = topk_smem;                                         // [kMaxK] (rank 0 gathers)
     uint32_t* hist = reinterpret_cast<uint32_t*>(topk_smem + kMaxK);              // [kMaxBins] this CTA's part
     uint32_t* comb = hist + kMaxBins;                                             // [kMaxBins] the cluster's sum
-    __shared__ uint32_t s_prefix, s_mask, s_need, s_count, s_total, s_bin, s_b, s_acc;
+    __shared__ uint32_t s_prefix, s_mask, s_need, s_count, s_total, s_bin, s_b, s_acc, s_sampled;
     __shared__ uint32_t s_warp[kThreadsTopk / 32];
     cg::cluster_group cl = cg::this_cluster();
     const int rank = (int)cl.block_rank();
@@ -150,17 +156,109 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreadsTopk)
     const int shifts[3] = {19, 8, 0};
     const int widths[3] = {13, 11, 8};
     bool fast = false;
+    // ---- a guess of the threshold from a sample of each part (the first 64
+    // scores of every 1024: contiguous runs, so that DRAM bursts are not
+    // wasted): the 24-bit key prefix tau whose keys and those above
+    // it number about kGuessFactor k in the sample, scaled to the row; found
+    // by a 13-bit histogram of the sample and then an 11-bit one of the sampled
+    // keys in the chosen bin (a second read of the sample, from L2).  The first
+    // pass then collects the keys whose prefix is >= tau as it counts.
+    uint32_t guess = 0xFFFFFFFFu;  // no guess: nothing is collected in the first pass
+    {
+        const int plen = end - beg;
+        // sampled float4s (or scores): j -> run j / 16 (64), item j % 16 (64)
+        const int ns = vec4 ? 16 * ((plen / 4) / 256) + min(16, (plen / 4) % 256)
+                            : 64 * (plen / 1024) + min(64, plen % 1024);
+        // f(key) for every sampled key, four loads in flight per thread
+        auto for_each_sample = [&](auto f) {
+            if (vec4) {
+                const float4* p4 = reinterpret_cast<const float4*>(part);
+                int j = tid;
+                for (; j + 3 * kThreadsTopk < ns; j += 4 * kThreadsTopk) {
+                    float4 v[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int jj = j + u * kThreadsTopk;
+                        v[u] = __ldg(p4 + (size_t)(jj >> 4) * 256 + (jj & 15));
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) { f(sort_key(v[u].x)); f(sort_key(v[u].y)); f(sort_key(v[u].z)); f(sort_key(v[u].w)); }
+                }
+                for (; j < ns; j += kThreadsTopk) {
+                    const float4 v = __ldg(p4 + (size_t)(j >> 4) * 256 + (j & 15));
+                    f(sort_key(v.x)); f(sort_key(v.y)); f(sort_key(v.z)); f(sort_key(v.w));
+                }
+            } else {
+                for (int j = tid; j < ns; j += kThreadsTopk) f(sort_key(__ldg(part + (size_t)(j >> 6) * 1024 + (j & 63))));
+            }
+        };
+        for (int i = tid; i < kMaxBins; i += kThreadsTopk) hist[i] = 0u;
+        if (tid == 0) s_sampled = (uint32_t)(vec4 ? 4 * ns : ns);
+        __syncthreads();
+        for_each_sample([&](uint32_t key) { if (key != 0u) atomicAdd(&hist[key >> 19], 1u); });
+        cl.sync();  // every part's sample histogram and size are complete
+        uint32_t sampled = 0;
+        for (int q = 0; q < kCluster; ++q) sampled += *cl.map_shared_rank(&s_sampled, q);
+        for (int i = tid; i < kMaxBins; i += kThreadsTopk) {
+            uint32_t v = 0;
+#pragma unroll
+            for (int q = 0; q < kCluster; ++q) v += cl.map_shared_rank(hist, q)[i];
+            comb[i] = v;
+        }
+        __syncthreads();
+        // the sample's share of kGuessFactor k, at least one key
+        const uint32_t want = (uint32_t)max(
+            1ll, ((long long)kGuessNum * k * sampled + (long long)kGuessDen * max(L, 1) - 1) /
+                     ((long long)kGuessDen * max(L, 1)));
+        find_bin(comb, kMaxBins, want, s_warp, &s_b, &s_acc, &s_total);
+        const uint32_t b1 = s_b, need1 = want - s_acc, tot = s_total;
+        cl.sync();  // the other parts have read this histogram before it is cleared
+        if (tot >= want) {  // uniform: enough valid sample keys to place tau
+            for (int i = tid; i < 2048; i += kThreadsTopk) hist[i] = 0u;
+            __syncthreads();
+            for_each_sample([&](uint32_t key) {
+                if (key != 0u && (key >> 19) == b1) atomicAdd(&hist[(key >> 8) & 0x7FFu], 1u);
+            });
+            cl.sync();
+            for (int i = tid; i < 2048; i += kThreadsTopk) {
+                uint32_t v = 0;
+#pragma unroll
+                for (int q = 0; q < kCluster; ++q) v += cl.map_shared_rank(hist, q)[i];
+                comb[i] = v;
+            }
+            __syncthreads();
+            find_bin(comb, 2048, need1, s_warp, &s_b, &s_acc, nullptr);
+            guess = (b1 << 11) | s_b;  // tau: the top 24 bits
+            cl.sync();  // the other parts have read this histogram before it is cleared
+        } else {
+            guess = 0u;  // the sample holds fewer valid keys than wanted: collect every valid key
+        }
+    }
 #pragma unroll 1
     for (int pass = 0; pass < 3; ++pass) {
         const int sh = shifts[pass], nb = 1 << widths[pass];
         for (int i = tid; i < nb; i += kThreadsTopk) hist[i] = 0u;
         __syncthreads();
         const uint32_t prefix = s_prefix, mask = s_mask;
-        for_each_score(part, end - beg, vec4, [&](float f, int) {
-            const uint32_t key = sort_key(f);
-            if (key != 0u && (key & mask) == prefix) atomicAdd(&hist[(key >> sh) & (uint32_t)(nb - 1)], 1u);
-        });
-        cl.sync();  // every part's histogram is complete (and rank 0's counter is zero)
+        if (pass == 0 && guess != 0xFFFFFFFFu) {
+            // count, and collect the keys at or above the guessed bin
+            for_each_score(part, end - beg, vec4, [&](float f, int i) {
+                const uint32_t key = sort_key(f);
+                if (key != 0u) {
+                    atomicAdd(&hist[key >> 19], 1u);
+                    if ((key >> 8) >= guess) {
+                        const uint32_t slot = atomicAdd(cnt0, 1u);
+                        if (slot < (uint32_t)kMaxK) sel0[slot] = sel_item(key, beg + i);
+                    }
+                }
+            });
+        } else {
+            for_each_score(part, end - beg, vec4, [&](float f, int) {
+                const uint32_t key = sort_key(f);
+                if (key != 0u && (key & mask) == prefix) atomicAdd(&hist[(key >> sh) & (uint32_t)(nb - 1)], 1u);
+            });
+        }
+        cl.sync();  // every part's histogram is complete (and rank 0's counter is settled)
         for (int i = tid; i < nb; i += kThreadsTopk) {
             uint32_t v = 0;
 #pragma unroll
@@ -178,6 +276,19 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreadsTopk)
             s_mask = mask | ((uint32_t)(nb - 1) << sh);
         }
         __syncthreads();
+        if (pass == 0 && guess != 0xFFFFFFFFu) {
+            // the guess held if it collected between min(k, valid keys) and
+            // kMaxK keys (rank 0's counter keeps counting past kMaxK)
+            const uint32_t n_spec = *cnt0;
+            if (n_spec >= min((uint32_t)k, s_total) && n_spec <= (uint32_t)kMaxK) {
+                fast = true;
+                break;
+            }
+            cl.sync();  // every part has read the counter
+            // a miss: rank 0's buffer is emptied before anything is collected again
+            if (tid == 0) s_count = 0u;
+            cl.sync();
+        }
         // keys at or above the bin: k - need above it, plus the bin's own
         const uint32_t at_or_above = (uint32_t)k - s_need + s_bin;
         const bool all_fit = pass == 0 && s_total <= (uint32_t)kMaxK;
@@ -232,24 +343,68 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreadsTopk)
     cl.sync();  // every part's keys sit in rank 0's buffer; no CTA reads another's memory after this
     if (rank != 0) return;
     const int n_sel = fast ? (int)min(s_count, (uint32_t)kMaxK) : k;
-    // ---- bitonic sort of the n_sel items, descending (padded with 0)
-    int n2 = 1;
-    while (n2 < n_sel) n2 <<= 1;
-    for (int i = n_sel + tid; i < n2; i += kThreadsTopk) sel[i] = 0ull;
+    // ---- sort of the n_sel items, descending (padded with 0 to kMaxK).  Each
+    // warp sorts its 128 items in registers (thread t holds items 4t .. 4t + 3;
+    // a bitonic network whose strides 1 and 2 pair items of one thread and 4 ..
+    // 64 items of one warp, through shuffles); then sorted lists are merged
+    // pairwise, 128 -> 256 -> ... -> kMaxK, through shared memory: an item's
+    // place in the merged list is its place in its own list plus the number of
+    // the other list's items before it (binary search; the first list goes
+    // first on equal values, so the places never collide).
+    static_assert(kMaxK == 4 * kThreadsTopk, "four items per thread");
+    for (int i = n_sel + tid; i < kMaxK; i += kThreadsTopk) sel[i] = 0ull;
     __syncthreads();
-    for (int size = 2; size <= n2; size <<= 1) {
+    unsigned long long x[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) x[u] = sel[4 * tid + u];
+    for (int size = 2; size <= 128; size <<= 1) {
         for (int stride2 = size >> 1; stride2 > 0; stride2 >>= 1) {
-            for (int i = tid; i < n2; i += kThreadsTopk) {
-                const int j = i ^ stride2;
-                if (j > i) {
-                    const bool desc = (i & size) == 0;
-                    const unsigned long long a = sel[i], b = sel[j];
-                    if (desc ? (a < b) : (a > b)) { sel[i] = b; sel[j] = a; }
+            if (stride2 >= 4) {  // partners in this warp: lane ^ (stride2 / 4)
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int i = 4 * tid + u, j = i ^ stride2;
+                    const unsigned long long y = __shfl_xor_sync(0xffffffffu, x[u], stride2 >> 2);
+                    const bool desc = size == 128 || (i & size) == 0, lower = i < j;
+                    x[u] = (desc == lower) ? (x[u] > y ? x[u] : y) : (x[u] < y ? x[u] : y);
                 }
+            } else {  // partners in this thread: (0, 2), (1, 3) for stride 2; (0, 1), (2, 3) for stride 1
+                auto cx = [&](unsigned long long& a, unsigned long long& b, int i) {  // i: a's index
+                    const bool desc = size == 128 || (i & size) == 0;
+                    if (desc ? (a < b) : (a > b)) { const unsigned long long t = a; a = b; b = t; }
+                };
+                if (stride2 == 2) { cx(x[0], x[2], 4 * tid); cx(x[1], x[3], 4 * tid + 1); }
+                else { cx(x[0], x[1], 4 * tid); cx(x[2], x[3], 4 * tid + 2); }
             }
-            __syncthreads();
         }
     }
+    unsigned long long* src = sel;
+    unsigned long long* dst = reinterpret_cast<unsigned long long*>(hist);  // hist + comb: 64 KB, idle now
+#pragma unroll
+    for (int u = 0; u < 4; ++u) src[4 * tid + u] = x[u];
+    __syncthreads();
+    for (int len = 128; len < kMaxK; len <<= 1) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int i = 4 * tid + u;
+            const int list = i / len, off = i - list * len;
+            const unsigned long long* other = src + (list ^ 1) * len;
+            const bool first = (list & 1) == 0;
+            // number of the other list's items placed before x: greater than x,
+            // or equal to it when the other list is the first
+            int lo = 0, hi = len;
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                const unsigned long long o = other[mid];
+                if (first ? (o > x[u]) : (o >= x[u])) lo = mid + 1; else hi = mid;
+            }
+            dst[(list & ~1) * len + off + lo] = x[u];
+        }
+        __syncthreads();
+        unsigned long long* t = src; src = dst; dst = t;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) x[u] = src[4 * tid + u];
+    }
+    sel = src;  // the sorted items
     const int n_out = min(n_sel, k);
     for (int i = tid; i < k; i += kThreadsTopk)
         out[(int64_t)r * k + i] = i < n_out ? (int32_t)~(uint32_t)(sel[i] & 0xFFFFFFFFull) : -1;
