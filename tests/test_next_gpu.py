@@ -141,3 +141,38 @@ def test_topk_many_ties_at_the_threshold(cuda_device):
     for k in (100, 4096):
         got = smla.topk_indices(s.cuda(), lens.cuda(), k).cpu().numpy()
         assert np.array_equal(got, O.topk_indices(s.numpy(), lens.numpy(), k))
+
+
+def test_topk_unaligned_rows_and_ordered_scores(cuda_device):
+    """Rows that do not start on a 16-byte boundary (a stride that is not a
+    multiple of 4 floats: the scalar path) and scores sorted along the row
+    (the sample must still place the threshold)."""
+    R, L, stride = 5, 50001, 50003
+    g = torch.Generator().manual_seed(61)
+    s = torch.randn((R, stride), generator=g)
+    s[1] = torch.arange(stride, dtype=torch.float32)          # ascending: the top k sit at the end
+    s[2] = -torch.arange(stride, dtype=torch.float32)         # descending: at the start
+    s[3, : stride // 2] = float("nan")                        # half the row never selectable
+    lens = torch.tensor([L, L, L, L, 77], dtype=torch.int32)
+    flat = s.cuda().contiguous()
+    for k in (1, 2048, 4096):
+        got = smla.smla_topk_indices  # raw entry point: stride in elements, unaligned rows
+        out = torch.empty((R, k), dtype=torch.int32, device="cuda")
+        st = got(flat.data_ptr(), stride, lens.cuda().data_ptr(), R, k, out.data_ptr(), 0)
+        assert st == smla.SMLA_OK
+        torch.cuda.synchronize()
+        assert np.array_equal(out.cpu().numpy(), O.topk_indices(s.numpy(), lens.numpy(), k)), k
+
+
+def test_topk_large_rows_sampled_guess(cuda_device):
+    """Rows of 4M scores (the sample keeps its density) from three
+    distributions, k = 2048, checked in full."""
+    R, L = 3, 4 << 20
+    g = torch.Generator(device="cuda").manual_seed(62)
+    s = torch.randn((R, L), generator=g, device="cuda")
+    s[1] = torch.rand((L,), generator=g, device="cuda")            # uniform
+    s[2] = torch.exp(4 * torch.randn((L,), generator=g, device="cuda"))  # heavy right tail
+    lens = torch.full((R,), L, dtype=torch.int32, device="cuda")
+    got = smla.topk_indices(s, lens, 2048).cpu().numpy()
+    ref = O.topk_indices(s.cpu().numpy(), lens.cpu().numpy(), 2048)
+    assert np.array_equal(got, ref)
