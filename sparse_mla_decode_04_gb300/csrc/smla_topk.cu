@@ -45,6 +45,7 @@ constexpr int kThreadsTopk = 1024;
 constexpr int kMaxK = SMLA_TOPK_MAX_K;
 constexpr int kMaxBins = 1 << 13;  // the first pass's histogram
 constexpr int kGuessNum = 29, kGuessDen = 20;  // kGuessFactor = 1.45: the guess aims at 1.45 k keys
+constexpr int kMaxTies = 1024;   // ties at the k-th key ranked directly (more: all collected keys sorted)
 constexpr int kCluster = 2;        // CTAs per row (a thread-block cluster), each over a contiguous part
 constexpr size_t kTopkSmem = kMaxK * 8 + 2 * kMaxBins * 4;  // selection + part and cluster histograms
 
@@ -342,67 +343,130 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreadsTopk)
     }
     cl.sync();  // every part's keys sit in rank 0's buffer; no CTA reads another's memory after this
     if (rank != 0) return;
-    const int n_sel = fast ? (int)min(s_count, (uint32_t)kMaxK) : k;
-    // ---- sort of the n_sel items, descending (padded with 0 to kMaxK).  Each
-    // warp sorts its 128 items in registers (thread t holds items 4t .. 4t + 3;
-    // a bitonic network whose strides 1 and 2 pair items of one thread and 4 ..
-    // 64 items of one warp, through shuffles); then sorted lists are merged
-    // pairwise, 128 -> 256 -> ... -> kMaxK, through shared memory: an item's
-    // place in the merged list is its place in its own list plus the number of
-    // the other list's items before it (binary search; the first list goes
-    // first on equal values, so the places never collide).
+    int n_sel = fast ? (int)min(s_count, (uint32_t)kMaxK) : k;
+    // ---- more than k collected: keep exactly the top k.  A radix select over
+    // the collected keys (11 + 11 + 10 bits, histograms in shared memory) gives
+    // the k-th largest key T; every key above T stays, and of the keys equal to
+    // T the need_eq with the smallest positions (each tie's rank among the ties
+    // counted directly; with more than kMaxTies ties all are sorted instead).
+    unsigned long long* kept = reinterpret_cast<unsigned long long*>(comb);  // [kMaxK / 2 ...]: 32 KB
+    if (n_sel > k) {
+        uint32_t prefix = 0u, mask = 0u, need = (uint32_t)k, count_t = 0u;
+        const int shs[3] = {21, 10, 0}, wds[3] = {11, 11, 10};
+#pragma unroll 1
+        for (int lvl = 0; lvl < 3; ++lvl) {
+            const int sh = shs[lvl], nb = 1 << wds[lvl];
+            for (int i = tid; i < nb; i += kThreadsTopk) hist[i] = 0u;
+            __syncthreads();
+            for (int i = tid; i < n_sel; i += kThreadsTopk) {
+                const uint32_t key = (uint32_t)(sel[i] >> 32);
+                if ((key & mask) == prefix) atomicAdd(&hist[(key >> sh) & (uint32_t)(nb - 1)], 1u);
+            }
+            __syncthreads();
+            find_bin(hist, nb, need, s_warp, &s_b, &s_acc, nullptr);
+            const uint32_t b = s_b;
+            need -= s_acc;
+            count_t = hist[b];
+            prefix |= b << sh;
+            mask |= (uint32_t)(nb - 1) << sh;
+            __syncthreads();  // hist read before the next level clears it
+        }
+        const uint32_t T = prefix, need_eq = need;  // 1 <= need_eq <= count_t
+        if (count_t == need_eq || count_t <= (uint32_t)kMaxTies) {
+            unsigned long long* ties = reinterpret_cast<unsigned long long*>(hist);  // [kMaxTies]
+            if (tid == 0) { s_count = 0u; s_acc = 0u; }
+            __syncthreads();
+            for (int i = tid; i < n_sel; i += kThreadsTopk) {
+                const unsigned long long it = sel[i];
+                const uint32_t key = (uint32_t)(it >> 32);
+                if (key > T || (key == T && count_t == need_eq)) kept[atomicAdd(&s_count, 1u)] = it;
+                else if (key == T) ties[atomicAdd(&s_acc, 1u)] = it;
+            }
+            __syncthreads();
+            if (count_t != need_eq) {  // the need_eq ties with the largest items (smallest positions)
+                const int nt = (int)s_acc;
+                for (int i = tid; i < nt; i += kThreadsTopk) {
+                    const unsigned long long it = ties[i];
+                    int rank = 0;
+                    for (int j = 0; j < nt; ++j) rank += ties[j] > it;
+                    if (rank < (int)need_eq) kept[atomicAdd(&s_count, 1u)] = it;
+                }
+                __syncthreads();
+            }
+            for (int i = tid; i < k; i += kThreadsTopk) sel[i] = kept[i];
+            __syncthreads();
+            n_sel = k;
+        }
+    }
+    // ---- sort of the n_sel items, descending (padded with 0 to n2, a power of
+    // two from 128 to kMaxK).  Each warp sorts its 128 items in registers
+    // (thread t holds items 4t .. 4t + 3; a bitonic network whose strides 1 and
+    // 2 pair items of one thread and 4 .. 64 items of one warp, through
+    // shuffles); then sorted lists are merged pairwise, 128 -> 256 -> ... -> n2,
+    // through shared memory: an item's place in the merged list is its place in
+    // its own list plus the number of the other list's items before it (binary
+    // search; the first list goes first on equal values, so the places never
+    // collide).  Threads past n2 / 4 hold nothing.
     static_assert(kMaxK == 4 * kThreadsTopk, "four items per thread");
-    for (int i = n_sel + tid; i < kMaxK; i += kThreadsTopk) sel[i] = 0ull;
+    int n2 = 128;
+    while (n2 < n_sel) n2 <<= 1;
+    const bool holds = 4 * tid < n2;  // whole warps (n2 >= 128)
+    for (int i = n_sel + tid; i < n2; i += kThreadsTopk) sel[i] = 0ull;
     __syncthreads();
     unsigned long long x[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) x[u] = sel[4 * tid + u];
-    for (int size = 2; size <= 128; size <<= 1) {
-        for (int stride2 = size >> 1; stride2 > 0; stride2 >>= 1) {
-            if (stride2 >= 4) {  // partners in this warp: lane ^ (stride2 / 4)
+    for (int u = 0; u < 4; ++u) x[u] = holds ? sel[4 * tid + u] : 0ull;
+    if (holds) {
+        for (int size = 2; size <= 128; size <<= 1) {
+            for (int stride2 = size >> 1; stride2 > 0; stride2 >>= 1) {
+                if (stride2 >= 4) {  // partners in this warp: lane ^ (stride2 / 4)
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int i = 4 * tid + u, j = i ^ stride2;
-                    const unsigned long long y = __shfl_xor_sync(0xffffffffu, x[u], stride2 >> 2);
-                    const bool desc = size == 128 || (i & size) == 0, lower = i < j;
-                    x[u] = (desc == lower) ? (x[u] > y ? x[u] : y) : (x[u] < y ? x[u] : y);
+                    for (int u = 0; u < 4; ++u) {
+                        const int i = 4 * tid + u, j = i ^ stride2;
+                        const unsigned long long y = __shfl_xor_sync(0xffffffffu, x[u], stride2 >> 2);
+                        const bool desc = size == 128 || (i & size) == 0, lower = i < j;
+                        x[u] = (desc == lower) ? (x[u] > y ? x[u] : y) : (x[u] < y ? x[u] : y);
+                    }
+                } else {  // partners in this thread: (0, 2), (1, 3) for stride 2; (0, 1), (2, 3) for stride 1
+                    auto cx = [&](unsigned long long& a, unsigned long long& b, int i) {  // i: a's index
+                        const bool desc = size == 128 || (i & size) == 0;
+                        if (desc ? (a < b) : (a > b)) { const unsigned long long t = a; a = b; b = t; }
+                    };
+                    if (stride2 == 2) { cx(x[0], x[2], 4 * tid); cx(x[1], x[3], 4 * tid + 1); }
+                    else { cx(x[0], x[1], 4 * tid); cx(x[2], x[3], 4 * tid + 2); }
                 }
-            } else {  // partners in this thread: (0, 2), (1, 3) for stride 2; (0, 1), (2, 3) for stride 1
-                auto cx = [&](unsigned long long& a, unsigned long long& b, int i) {  // i: a's index
-                    const bool desc = size == 128 || (i & size) == 0;
-                    if (desc ? (a < b) : (a > b)) { const unsigned long long t = a; a = b; b = t; }
-                };
-                if (stride2 == 2) { cx(x[0], x[2], 4 * tid); cx(x[1], x[3], 4 * tid + 1); }
-                else { cx(x[0], x[1], 4 * tid); cx(x[2], x[3], 4 * tid + 2); }
             }
         }
     }
     unsigned long long* src = sel;
     unsigned long long* dst = reinterpret_cast<unsigned long long*>(hist);  // hist + comb: 64 KB, idle now
 #pragma unroll
-    for (int u = 0; u < 4; ++u) src[4 * tid + u] = x[u];
+    for (int u = 0; u < 4; ++u)
+        if (holds) src[4 * tid + u] = x[u];
     __syncthreads();
-    for (int len = 128; len < kMaxK; len <<= 1) {
+    for (int len = 128; len < n2; len <<= 1) {
+        if (holds) {
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int i = 4 * tid + u;
-            const int list = i / len, off = i - list * len;
-            const unsigned long long* other = src + (list ^ 1) * len;
-            const bool first = (list & 1) == 0;
-            // number of the other list's items placed before x: greater than x,
-            // or equal to it when the other list is the first
-            int lo = 0, hi = len;
-            while (lo < hi) {
-                const int mid = (lo + hi) >> 1;
-                const unsigned long long o = other[mid];
-                if (first ? (o > x[u]) : (o >= x[u])) lo = mid + 1; else hi = mid;
+            for (int u = 0; u < 4; ++u) {
+                const int i = 4 * tid + u;
+                const int list = i / len, off = i - list * len;
+                const unsigned long long* other = src + (list ^ 1) * len;
+                const bool first = (list & 1) == 0;
+                // number of the other list's items placed before x: greater than
+                // x, or equal to it when the other list is the first
+                int lo = 0, hi = len;
+                while (lo < hi) {
+                    const int mid = (lo + hi) >> 1;
+                    const unsigned long long o = other[mid];
+                    if (first ? (o > x[u]) : (o >= x[u])) lo = mid + 1; else hi = mid;
+                }
+                dst[(list & ~1) * len + off + lo] = x[u];
             }
-            dst[(list & ~1) * len + off + lo] = x[u];
         }
         __syncthreads();
         unsigned long long* t = src; src = dst; dst = t;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) x[u] = src[4 * tid + u];
+        for (int u = 0; u < 4; ++u) x[u] = holds ? src[4 * tid + u] : 0ull;
     }
     sel = src;  // the sorted items
     const int n_out = min(n_sel, k);
