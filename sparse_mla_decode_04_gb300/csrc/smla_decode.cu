@@ -1463,7 +1463,10 @@ __device__ void plan_warp(const KParams& p, int pair, int n_pairs, UnitDesc* uni
         const int units_c = s_prefix[R];
         const long long passes_c = (units_c + n_pairs - 1) / n_pairs;
         const long long mk_c = (long long)chunk * passes_c + kUnitCostTiles * passes_c;
-        stream = stream_ok && Q > min(units_c, n_pairs) && mk_s < mk_c;
+        // Also over several passes: a chunk count that leaves the last pass
+        // part-empty costs the chunked plan up to a whole chunk of imbalance and
+        // many partials, which one range per pair avoids.
+        stream = stream_ok && mk_s < mk_c;
     }
     if (stream) {
         // per-row unit counts of the stream plan, then (in place) their prefix: unit ids
