@@ -1122,7 +1122,10 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, UnitDesc* units, in
             // issue stream) produced this tile's scores.
             float ps_side = 0.f, lo_side = 0.f;
             if (ok) {
-                float sm[4] = {0.f, 0.f, 0.f, 0.f}, la[4] = {0.f, 0.f, 0.f, 0.f};
+                // pairs of entries in packed fp32x2 arithmetic (each lane of it
+                // rounds as the scalar operation would)
+                const uint64_t qs2 = f2_pack(qscale, qscale), nm2 = f2_pack(-msub, -msub);
+                uint64_t sm2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)}, la2[2] = {sm2[0], sm2[0]};
 #pragma unroll 1
                 for (int q = 0; q < 2; ++q) {
                     uint32_t v[16];
@@ -1132,29 +1135,36 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, UnitDesc* units, in
                     uint32_t hl[16];  // hi pairs, then lo pairs
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
-                        float x0 = fmaf(__uint_as_float(v[2 * j]), qscale, -msub);
-                        float x1 = fmaf(__uint_as_float(v[2 * j + 1]), qscale, -msub);
+                        float x0, x1;
+                        f2_unpack(f2_fma(f2_pack(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1])), qs2, nm2), x0,
+                                  x1);
                         if (vq != 0xFFFFu) {
                             x0 = ((vq >> (2 * j)) & 1u) ? x0 : -INFINITY;
                             x1 = ((vq >> (2 * j + 1)) & 1u) ? x1 : -INFINITY;
                         }
                         const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-                        sm[j & 3] += p0 + p1;
+                        const uint64_t p2 = f2_pack(p0, p1);
+                        sm2[j & 1] = f2_add(sm2[j & 1], p2);
                         const __nv_bfloat162 hb = __floats2bfloat162_rn(p0, p1);
                         memcpy(&hl[j], &hb, 4);
                         if (cold) {
                             hl[8 + j] = 0u;
                         } else {
-                            const float r0 = p0 - __low2float(hb), r1 = p1 - __high2float(hb);
+                            const uint64_t r2 = f2_sub(p2, f2_pack(__low2float(hb), __high2float(hb)));
+                            float r0, r1;
+                            f2_unpack(r2, r0, r1);
                             hl[8 + j] = pack_bf16(r0, r1);
-                            la[j & 3] += fabsf(r0) + fabsf(r1);
+                            la2[j & 1] = f2_add(la2[j & 1], f2_pack(fabsf(r0), fabsf(r1)));
                         }
                     }
                     tmem_st16(ts + 16 * q, hl);
                 }
-                ps_side = (sm[0] + sm[1]) + (sm[2] + sm[3]);
+                float a0, a1, b0, b1;
+                f2_unpack(f2_add(sm2[0], sm2[1]), a0, a1);
+                ps_side = a0 + a1;
+                f2_unpack(f2_add(la2[0], la2[1]), b0, b1);
                 // |bf16(r)| <= |r| (1 + 2^-8): a bound on the sum of |lo|
-                lo_side = cold ? (sd == 0 ? cap0 : cap1) : ((la[0] + la[1]) + (la[2] + la[3])) * (1.0f + 1.0f / 256.0f);
+                lo_side = cold ? (sd == 0 ? cap0 : cap1) : (b0 + b1) * (1.0f + 1.0f / 256.0f);
             }
             st_shared_f32(xch_addr(1, sd), ps_side);
             st_shared_f32(xch_addr(2, sd), lo_side);
