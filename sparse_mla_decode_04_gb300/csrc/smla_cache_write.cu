@@ -64,11 +64,25 @@ __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// Every NaN of two bf16 values becomes 0x7FC0, both halves at once: for a
+// magnitude m <= 0x7FFF, bit 15 of m + 0x7F is set iff m > 0x7F80 (a NaN), and
+// the low half's sum never carries into the high half.
 __device__ __forceinline__ uint32_t canon_nan_bf16x2(uint32_t w) {
-    uint32_t lo = w & 0xFFFFu, hi = w >> 16;
-    if ((lo & 0x7FFFu) > 0x7F80u) lo = 0x7FC0u;
-    if ((hi & 0x7FFFu) > 0x7F80u) hi = 0x7FC0u;
-    return lo | (hi << 16);
+    const uint32_t nan = ((w & 0x7FFF7FFFu) + 0x007F007Fu) & 0x80008000u;
+    const uint32_t mask = (nan >> 15) * 0xFFFFu;
+    return (w & ~mask) | (0x7FC07FC0u & mask);
+}
+
+// Two products a * f, b * f in one packed fp32x2 multiply (each lane rounds
+// as the scalar multiply does).
+__device__ __forceinline__ float2 mul2(float a, float b, float f) {
+    uint64_t x, y, r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a), "f"(b));
+    asm("mov.b64 %0, {%1, %1};" : "=l"(y) : "f"(f));
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(x), "l"(y));
+    float2 o;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(o.x), "=f"(o.y) : "l"(r));
+    return o;
 }
 
 // One row: w holds this lane's 16 dims (dims 16 lane .. 16 lane + 15).
@@ -94,9 +108,11 @@ __device__ __forceinline__ void write_row(const uint32_t (&w)[8], int lane, uint
         const float f = inv_scale(code);
         uint32_t o[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-            o[i] = e4m3x4(bf16_lo(w[2 * i]) * f, bf16_hi(w[2 * i]) * f, bf16_lo(w[2 * i + 1]) * f,
-                          bf16_hi(w[2 * i + 1]) * f);
+        for (int i = 0; i < 4; ++i) {
+            const float2 p0 = mul2(bf16_lo(w[2 * i]), bf16_hi(w[2 * i]), f);
+            const float2 p1 = mul2(bf16_lo(w[2 * i + 1]), bf16_hi(w[2 * i + 1]), f);
+            o[i] = e4m3x4(p0.x, p0.y, p1.x, p1.y);
+        }
         __stcs(reinterpret_cast<uint4*>(dst + 16 * lane), make_uint4(o[0], o[1], o[2], o[3]));
     } else {
         uint4 r0, r1;
@@ -108,13 +124,12 @@ __device__ __forceinline__ void write_row(const uint32_t (&w)[8], int lane, uint
         __stcs(rd, r0);
         __stcs(rd + 1, r1);
     }
-    // the 7 codes (lanes 0, 4, ..., 24) and a zero pad byte, one 8-byte store
-    uint32_t lo = 0, hi = 0;
-#pragma unroll
-    for (int g = 0; g < 7; ++g) {
-        const uint32_t cg = __shfl_sync(0xffffffffu, code, 4 * g);
-        if (g < 4) lo |= cg << (8 * g); else hi |= cg << (8 * (g - 4));
-    }
+    // the 7 codes (held by lanes 0, 4, ..., 24) and a zero pad byte, one 8-byte
+    // store: group g's first lane places its code at byte g of the pair
+    const int g = lane >> 2;
+    const bool first = (lane & 3) == 0 && g < 7;
+    const uint32_t lo = __reduce_or_sync(0xffffffffu, (first && g < 4) ? code << (8 * g) : 0u);
+    const uint32_t hi = __reduce_or_sync(0xffffffffu, (first && g >= 4) ? code << (8 * (g - 4)) : 0u);
     if (lane == 0) *reinterpret_cast<uint2*>(sdst) = make_uint2(lo, hi);
 }
 
