@@ -15,11 +15,11 @@
 //
 // Usually one read of the row: a sample (the first 64 scores of every 1024)
 // places a 24-bit key prefix tau that about 1.45 k keys reach; the first pass
-// counts the 13-bit histogram of the row and collects every key whose prefix
-// is >= tau.  When that collected between k (or every valid key) and
-// SMLA_TOPK_MAX_K keys, they hold the top k: the pass ends there.  Otherwise
-// the radix select goes on (13 + 11 + 8 key bits, the bin of the k-th largest
-// key found by a block-wide suffix scan): as soon as the keys at or above the
+// collects every key whose prefix is >= tau and counts the valid keys.  When
+// that collected between k (or every valid key) and SMLA_TOPK_MAX_K keys, they
+// hold the top k.  Otherwise a radix select runs over the row (13 + 11 + 8 key
+// bits, the bin of the k-th largest key found by a block-wide suffix scan): as
+// soon as the keys at or above the
 // current bin number at most SMLA_TOPK_MAX_K, one more pass collects exactly
 // those; with many keys tied at the threshold, the third pass gives the k-th
 // largest key T and a collecting pass takes every key above T and, in
@@ -138,7 +138,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreadsTopk)
     unsigned long long* sel = topk_smem;                                         // [kMaxK] (rank 0 gathers)
     uint32_t* hist = reinterpret_cast<uint32_t*>(topk_smem + kMaxK);              // [kMaxBins] this CTA's part
     uint32_t* comb = hist + kMaxBins;                                             // [kMaxBins] the cluster's sum
-    __shared__ uint32_t s_prefix, s_mask, s_need, s_count, s_total, s_bin, s_b, s_acc, s_sampled;
+    __shared__ uint32_t s_prefix, s_mask, s_need, s_count, s_total, s_bin, s_b, s_acc, s_sampled, s_valid;
     __shared__ uint32_t s_warp[kThreadsTopk / 32];
     cg::cluster_group cl = cg::this_cluster();
     const int rank = (int)cl.block_rank();
@@ -153,7 +153,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreadsTopk)
     // rank 0's counter and selection buffer, which every CTA of the cluster fills
     uint32_t* cnt0 = cl.map_shared_rank(&s_count, 0);
     unsigned long long* sel0 = cl.map_shared_rank(sel, 0);
-    if (tid == 0) { s_prefix = 0u; s_mask = 0u; s_need = (uint32_t)k; s_count = 0u; }
+    if (tid == 0) { s_prefix = 0u; s_mask = 0u; s_need = (uint32_t)k; s_count = 0u; s_valid = 0u; }
     const int shifts[3] = {19, 8, 0};
     const int widths[3] = {13, 11, 8};
     bool fast = false;
@@ -163,7 +163,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreadsTopk)
     // it number about kGuessFactor k in the sample, scaled to the row; found
     // by a 13-bit histogram of the sample and then an 11-bit one of the sampled
     // keys in the chosen bin (a second read of the sample, from L2).  The first
-    // pass then collects the keys whose prefix is >= tau as it counts.
+    // pass then collects the keys whose prefix is >= tau.
     uint32_t guess = 0xFFFFFFFFu;  // no guess: nothing is collected in the first pass
     {
         const int plen = end - beg;
@@ -235,31 +235,45 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreadsTopk)
             guess = 0u;  // the sample holds fewer valid keys than wanted: collect every valid key
         }
     }
+    if (guess != 0xFFFFFFFFu) {
+        // collect the keys at or above the guessed prefix, and count the valid keys
+        uint32_t nvalid = 0u;
+        for_each_score(part, end - beg, vec4, [&](float f, int i) {
+            const uint32_t key = sort_key(f);
+            nvalid += key != 0u ? 1u : 0u;
+            if (key != 0u && (key >> 8) >= guess) {
+                const uint32_t slot = atomicAdd(cnt0, 1u);
+                if (slot < (uint32_t)kMaxK) sel0[slot] = sel_item(key, beg + i);
+            }
+        });
+        nvalid = __reduce_add_sync(0xffffffffu, nvalid);
+        if ((tid & 31) == 0) atomicAdd(&s_valid, nvalid);
+        cl.sync();  // every part's keys and valid count are in (rank 0's counter is settled)
+        uint32_t valid = 0u;
+        for (int q = 0; q < kCluster; ++q) valid += *cl.map_shared_rank(&s_valid, q);
+        // the guess held if it collected between min(k, valid keys) and
+        // kMaxK keys (rank 0's counter keeps counting past kMaxK)
+        const uint32_t n_spec = *cnt0;
+        if (n_spec >= min((uint32_t)k, valid) && n_spec <= (uint32_t)kMaxK) {
+            fast = true;
+        } else {
+            cl.sync();  // every part has read the counter
+            // a miss: rank 0's buffer is emptied before anything is collected again
+            if (tid == 0) s_count = 0u;
+            cl.sync();
+        }
+    }
 #pragma unroll 1
-    for (int pass = 0; pass < 3; ++pass) {
+    for (int pass = 0; pass < 3 && !fast; ++pass) {
         const int sh = shifts[pass], nb = 1 << widths[pass];
         for (int i = tid; i < nb; i += kThreadsTopk) hist[i] = 0u;
         __syncthreads();
         const uint32_t prefix = s_prefix, mask = s_mask;
-        if (pass == 0 && guess != 0xFFFFFFFFu) {
-            // count, and collect the keys at or above the guessed bin
-            for_each_score(part, end - beg, vec4, [&](float f, int i) {
-                const uint32_t key = sort_key(f);
-                if (key != 0u) {
-                    atomicAdd(&hist[key >> 19], 1u);
-                    if ((key >> 8) >= guess) {
-                        const uint32_t slot = atomicAdd(cnt0, 1u);
-                        if (slot < (uint32_t)kMaxK) sel0[slot] = sel_item(key, beg + i);
-                    }
-                }
-            });
-        } else {
-            for_each_score(part, end - beg, vec4, [&](float f, int) {
-                const uint32_t key = sort_key(f);
-                if (key != 0u && (key & mask) == prefix) atomicAdd(&hist[(key >> sh) & (uint32_t)(nb - 1)], 1u);
-            });
-        }
-        cl.sync();  // every part's histogram is complete (and rank 0's counter is settled)
+        for_each_score(part, end - beg, vec4, [&](float f, int) {
+            const uint32_t key = sort_key(f);
+            if (key != 0u && (key & mask) == prefix) atomicAdd(&hist[(key >> sh) & (uint32_t)(nb - 1)], 1u);
+        });
+        cl.sync();  // every part's histogram is complete
         for (int i = tid; i < nb; i += kThreadsTopk) {
             uint32_t v = 0;
 #pragma unroll
@@ -277,19 +291,6 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreadsTopk)
             s_mask = mask | ((uint32_t)(nb - 1) << sh);
         }
         __syncthreads();
-        if (pass == 0 && guess != 0xFFFFFFFFu) {
-            // the guess held if it collected between min(k, valid keys) and
-            // kMaxK keys (rank 0's counter keeps counting past kMaxK)
-            const uint32_t n_spec = *cnt0;
-            if (n_spec >= min((uint32_t)k, s_total) && n_spec <= (uint32_t)kMaxK) {
-                fast = true;
-                break;
-            }
-            cl.sync();  // every part has read the counter
-            // a miss: rank 0's buffer is emptied before anything is collected again
-            if (tid == 0) s_count = 0u;
-            cl.sync();
-        }
         // keys at or above the bin: k - need above it, plus the bin's own
         const uint32_t at_or_above = (uint32_t)k - s_need + s_bin;
         const bool all_fit = pass == 0 && s_total <= (uint32_t)kMaxK;
