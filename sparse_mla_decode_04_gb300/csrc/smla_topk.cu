@@ -15,9 +15,10 @@
 //
 // Usually one read of the row: a sample (the first 64 scores of every 1024)
 // places a 24-bit key prefix tau that about 1.45 k keys reach; the first pass
-// collects every key whose prefix is >= tau and counts the valid keys.  When
-// that collected between k (or every valid key) and SMLA_TOPK_MAX_K keys, they
-// hold the top k.  Otherwise a radix select runs over the row (13 + 11 + 8 key
+// collects every key whose prefix is >= tau (one float comparison per score).
+// When that collected between k and SMLA_TOPK_MAX_K keys (or, with tau = 0,
+// every valid key), they hold the top k.  Otherwise a radix select runs over
+// the row (13 + 11 + 8 key
 // bits, the bin of the k-th largest key found by a block-wide suffix scan): as
 // soon as the keys at or above the
 // current bin number at most SMLA_TOPK_MAX_K, one more pass collects exactly
@@ -55,6 +56,16 @@ __device__ __forceinline__ uint32_t sort_key(float f) {
     if (f != f) return 0u;
     const uint32_t b = f == 0.f ? 0u : __float_as_uint(f);
     return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+constexpr uint32_t kKeyNegInf = 0x007FFFFFu;  // sort_key(-inf): every key below it is a NaN's bit pattern
+
+// The float whose key is `key` (key >= kKeyNegInf): for a score f that is not
+// NaN, sort_key(f) >= key exactly when f >= key_float(key) (the keys follow
+// the float order, and -0 >= +0 as their shared key requires); a NaN fails
+// the comparison, as its key 0 would.
+__device__ __forceinline__ float key_float(uint32_t key) {
+    return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
 }
 
 // Calls f(score, position) for every position of [0, L) of `row`: 16-byte
@@ -138,7 +149,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreadsTopk)
     unsigned long long* sel = topk_smem;                                         // [kMaxK] (rank 0 gathers)
     uint32_t* hist = reinterpret_cast<uint32_t*>(topk_smem + kMaxK);              // [kMaxBins] this CTA's part
     uint32_t* comb = hist + kMaxBins;                                             // [kMaxBins] the cluster's sum
-    __shared__ uint32_t s_prefix, s_mask, s_need, s_count, s_total, s_bin, s_b, s_acc, s_sampled, s_valid;
+    __shared__ uint32_t s_prefix, s_mask, s_need, s_count, s_total, s_bin, s_b, s_acc, s_sampled;
     __shared__ uint32_t s_warp[kThreadsTopk / 32];
     cg::cluster_group cl = cg::this_cluster();
     const int rank = (int)cl.block_rank();
@@ -153,7 +164,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreadsTopk)
     // rank 0's counter and selection buffer, which every CTA of the cluster fills
     uint32_t* cnt0 = cl.map_shared_rank(&s_count, 0);
     unsigned long long* sel0 = cl.map_shared_rank(sel, 0);
-    if (tid == 0) { s_prefix = 0u; s_mask = 0u; s_need = (uint32_t)k; s_count = 0u; s_valid = 0u; }
+    if (tid == 0) { s_prefix = 0u; s_mask = 0u; s_need = (uint32_t)k; s_count = 0u; }
     const int shifts[3] = {19, 8, 0};
     const int widths[3] = {13, 11, 8};
     bool fast = false;
@@ -236,25 +247,22 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreadsTopk)
         }
     }
     if (guess != 0xFFFFFFFFu) {
-        // collect the keys at or above the guessed prefix, and count the valid keys
-        uint32_t nvalid = 0u;
+        // collect the valid keys whose prefix is >= tau: the scores >= the float
+        // of key max(tau << 8, the key of -inf) (tau = 0: every valid key)
+        const float fthr = key_float(max(guess << 8, kKeyNegInf));
         for_each_score(part, end - beg, vec4, [&](float f, int i) {
-            const uint32_t key = sort_key(f);
-            nvalid += key != 0u ? 1u : 0u;
-            if (key != 0u && (key >> 8) >= guess) {
+            if (f >= fthr) {
                 const uint32_t slot = atomicAdd(cnt0, 1u);
-                if (slot < (uint32_t)kMaxK) sel0[slot] = sel_item(key, beg + i);
+                if (slot < (uint32_t)kMaxK) sel0[slot] = sel_item(sort_key(f), beg + i);
             }
         });
-        nvalid = __reduce_add_sync(0xffffffffu, nvalid);
-        if ((tid & 31) == 0) atomicAdd(&s_valid, nvalid);
-        cl.sync();  // every part's keys and valid count are in (rank 0's counter is settled)
-        uint32_t valid = 0u;
-        for (int q = 0; q < kCluster; ++q) valid += *cl.map_shared_rank(&s_valid, q);
-        // the guess held if it collected between min(k, valid keys) and
-        // kMaxK keys (rank 0's counter keeps counting past kMaxK)
+        cl.sync();  // every part's keys are in (rank 0's counter is settled)
+        // the guess held if it collected between k and kMaxK keys, or with tau = 0
+        // every valid key, at most kMaxK (rank 0's counter keeps counting past
+        // kMaxK); a row with fewer than k valid keys at a tau above 0 takes the
+        // radix select
         const uint32_t n_spec = *cnt0;
-        if (n_spec >= min((uint32_t)k, valid) && n_spec <= (uint32_t)kMaxK) {
+        if ((n_spec >= (uint32_t)k || guess == 0u) && n_spec <= (uint32_t)kMaxK) {
             fast = true;
         } else {
             cl.sync();  // every part has read the counter
