@@ -69,7 +69,7 @@ __device__ __forceinline__ float key_float(uint32_t key) {
 }
 
 // Calls f(score, position) for every position of [0, L) of `row`: 16-byte
-// loads where the row is 16-byte aligned, four of them in flight per thread.
+// loads where the row is 16-byte aligned, eight of them in flight per thread.
 template <class F>
 __device__ __forceinline__ void for_each_score(const float* __restrict__ row, int L, bool vec4, F f) {
     const int tid = threadIdx.x;
@@ -77,12 +77,12 @@ __device__ __forceinline__ void for_each_score(const float* __restrict__ row, in
         const float4* row4 = reinterpret_cast<const float4*>(row);
         const int n4 = L / 4;
         int i = tid;
-        for (; i + 3 * kThreadsTopk < n4; i += 4 * kThreadsTopk) {
-            float4 v[4];
+        for (; i + 7 * kThreadsTopk < n4; i += 8 * kThreadsTopk) {
+            float4 v[8];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) v[u] = __ldg(row4 + i + u * kThreadsTopk);
+            for (int u = 0; u < 8; ++u) v[u] = __ldg(row4 + i + u * kThreadsTopk);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < 8; ++u) {
                 const int b = 4 * (i + u * kThreadsTopk);
                 f(v[u].x, b); f(v[u].y, b + 1); f(v[u].z, b + 2); f(v[u].w, b + 3);
             }
