@@ -181,20 +181,20 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreadsTopk)
         // sampled float4s (or scores): j -> run j / 16 (64), item j % 16 (64)
         const int ns = vec4 ? 16 * ((plen / 4) / 256) + min(16, (plen / 4) % 256)
                             : 64 * (plen / 1024) + min(64, plen % 1024);
-        // f(key) for every sampled key, four loads in flight per thread
+        // f(key) for every sampled key, eight loads in flight per thread
         auto for_each_sample = [&](auto f) {
             if (vec4) {
                 const float4* p4 = reinterpret_cast<const float4*>(part);
                 int j = tid;
-                for (; j + 3 * kThreadsTopk < ns; j += 4 * kThreadsTopk) {
-                    float4 v[4];
+                for (; j + 7 * kThreadsTopk < ns; j += 8 * kThreadsTopk) {
+                    float4 v[8];
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
+                    for (int u = 0; u < 8; ++u) {
                         const int jj = j + u * kThreadsTopk;
                         v[u] = __ldg(p4 + (size_t)(jj >> 4) * 256 + (jj & 15));
                     }
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) { f(sort_key(v[u].x)); f(sort_key(v[u].y)); f(sort_key(v[u].z)); f(sort_key(v[u].w)); }
+                    for (int u = 0; u < 8; ++u) { f(sort_key(v[u].x)); f(sort_key(v[u].y)); f(sort_key(v[u].z)); f(sort_key(v[u].w)); }
                 }
                 for (; j < ns; j += kThreadsTopk) {
                     const float4 v = __ldg(p4 + (size_t)(j >> 4) * 256 + (j & 15));
