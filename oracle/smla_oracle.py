@@ -83,9 +83,11 @@ def ue8m0_scale(code):
 
 
 def bf16_bits_to_f64(bits) -> np.ndarray:
-    """bf16 is the upper half of an IEEE binary32."""
+    """bf16 is the upper half of an IEEE binary32.  NaN patterns are valid
+    inputs (they stay NaN; the widening only warns about signalling ones)."""
     b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
-    return b.view(np.float32).astype(np.float64)
+    with np.errstate(invalid="ignore"):
+        return b.view(np.float32).astype(np.float64)
 
 
 # ---------------------------------------------------------------------------
