@@ -232,8 +232,8 @@ smla_status smla_cache_write(const void* latent, int64_t num_rows, const int64_t
 
 /*
  * Top-k producer: the decode's top-k index list from per-position scores.
- * The pages name this step (the indexer top-k path whose cp-gather the vLLM
- * page's comment "8k/1k TP8 follow-up", item 2, reworks) but not how its
+ * The vLLM page names this step (the indexer top-k path whose cp-gather its
+ * comment "8k/1k TP8 follow-up", item 2, reworks) but not how its
  * scores are made, so the scores are an input.  For each row r:
  * out[r][0 .. k-1] = the positions p in [0, min(lens[r], stride)) with the
  * largest scores[r][p], ordered by score descending and then by position
@@ -257,8 +257,8 @@ smla_status smla_topk_indices(const float* scores, int64_t stride, const int32_t
 #define SMLA_STATIC_SCRATCH_BYTES (48u * 1024u * 1024u)
 
 /*
- * smla_decode for callers that cannot allocate device memory.  The pages have
- * no counterpart to this entry point.
+ * smla_decode for callers that cannot allocate device memory.  The cited
+ * pull-request pages have no counterpart to this entry point.
  *
  * Some callers have no way to call cudaMalloc: plugin or custom-op interfaces
  * that hand a kernel only its inputs, outputs and a stream; code that runs

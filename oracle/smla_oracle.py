@@ -17,8 +17,7 @@ can be checked against the sources by eye:
   (the split-count cost model) and part 2 (split rows merged from fp32
   partials plus LSE).
 
-Readings taken where the pages are silent (each is also listed in the design
-notes): the sink is a logit in the already-scaled domain; the returned LSE is
+Readings taken where the cited pull-request pages are silent: the sink is a logit in the already-scaled domain; the returned LSE is
 natural-log and includes the sink; top-k / window / compressed entries form a
 multiset (no de-duplication); V is the whole 512-wide dequantised entry; the
 dim order is [NoPE 0..447 | RoPE 448..511]; scale g covers NoPE dims
@@ -311,7 +310,7 @@ def plan_num_splits(num_rows: int, num_heads: int, kv_len: int, coeffs: dict, s_
 # "[ROCm][DSV4][Perf] Optimize Triton sparse-MLA decode on gfx950", section
 # "Design", last paragraph: the cache writers store NoPE dims as FP8 with one
 # UE8M0 scale per 64 dims, cap the UE8M0 codes at 254 and canonicalise RoPE
-# NaNs.  Readings (stated in the design notes): the scale of a group is the
+# NaNs.  Readings: the scale of a group is the
 # smallest power of two that brings the group's largest magnitude within the
 # e4m3 range (448); codes are clamped to [0, 254]; values are rounded to
 # nearest, ties to even, saturating at +-448; a NaN NoPE value is stored as
@@ -394,8 +393,8 @@ def cache_write(latent_bits, slots, pool, scales):
 # top-k selection: the producer of main_idx
 # ---------------------------------------------------------------------------
 # The step before the decode: each row's top-k index list (-1 = invalid slot)
-# is the k positions of [0, L_r) with the largest scores.  The pages name the
-# producer (the indexer top-k path and its cp-gather, "8k/1k TP8 follow-up",
+# is the k positions of [0, L_r) with the largest scores.  The vLLM page names
+# the producer (the indexer top-k path and its cp-gather, "8k/1k TP8 follow-up",
 # item 2) but not how scores are made, so scores are an input here.
 # Readings: order by score descending, ties by position ascending; NaN scores
 # are never selected; rows with fewer than k selectable positions are padded

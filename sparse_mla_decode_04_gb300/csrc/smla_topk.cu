@@ -1,8 +1,8 @@
 // Top-k selection: per row, the k positions of [0, len_r) with the largest
 // scores -- the decode's top-k index list (-1 = invalid slot).
 //
-// The pages name this producer (the indexer top-k path whose cp-gather is
-// reworked in "[ROCm][DSV4][Perf] Optimize Triton sparse-MLA decode on
+// The cited page names this producer (the indexer top-k path whose cp-gather
+// is reworked in "[ROCm][DSV4][Perf] Optimize Triton sparse-MLA decode on
 // gfx950", comment "8k/1k TP8 follow-up", item 2) but not how the scores are
 // made, so the scores are an input.  Order: score descending, ties by position
 // ascending; NaN scores are never selected; a row with fewer than k
