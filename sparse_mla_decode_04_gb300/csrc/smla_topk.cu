@@ -25,9 +25,9 @@
 // those; with many keys tied at the threshold, the third pass gives the k-th
 // largest key T and a collecting pass takes every key above T and, in
 // position order (the second half's ties after the first's), the first
-// positions equal to T.  The collected keys are sorted in shared memory (key
-// descending, position ascending): each warp sorts 128 in registers, then
-// merge-path merges join the sorted lists.
+// positions equal to T.  The selected keys are sorted (key descending,
+// position ascending) by a bitonic network over the block: registers and
+// shuffles within a warp, shared memory across warps.
 #include <atomic>
 #include <cstdint>
 #include <mutex>
@@ -408,37 +408,56 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreadsTopk)
         }
     }
     // ---- sort of the n_sel items, descending (padded with 0 to n2, a power of
-    // two from 128 to kMaxK).  Each warp sorts its 128 items in registers
-    // (thread t holds items 4t .. 4t + 3; a bitonic network whose strides 1 and
-    // 2 pair items of one thread and 4 .. 64 items of one warp, through
-    // shuffles); then sorted lists are merged pairwise, 128 -> 256 -> ... -> n2,
-    // through shared memory: an item's place in the merged list is its place in
-    // its own list plus the number of the other list's items before it (binary
-    // search; the first list goes first on equal values, so the places never
-    // collide).  Threads past n2 / 4 hold nothing.
+    // two from 128 to kMaxK): a bitonic network over the block.  Thread t holds
+    // items 4t .. 4t + 3 in registers; compare-exchange steps of stride 1 and 2
+    // pair items of one thread, strides 4 .. 64 items of one warp (through
+    // shuffles), and strides of 128 and more items of other warps, through
+    // shared memory (two buffers used in turn, so one barrier per step: a
+    // buffer is written again only after the step between has made every
+    // thread finish reading it).  Threads past n2 / 4 hold nothing (whole
+    // warps, as n2 >= 128).
     static_assert(kMaxK == 4 * kThreadsTopk, "four items per thread");
     int n2 = 128;
     while (n2 < n_sel) n2 <<= 1;
-    const bool holds = 4 * tid < n2;  // whole warps (n2 >= 128)
+    const bool holds = 4 * tid < n2;
     for (int i = n_sel + tid; i < n2; i += kThreadsTopk) sel[i] = 0ull;
     __syncthreads();
     unsigned long long x[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) x[u] = holds ? sel[4 * tid + u] : 0ull;
-    if (holds) {
-        for (int size = 2; size <= 128; size <<= 1) {
-            for (int stride2 = size >> 1; stride2 > 0; stride2 >>= 1) {
+    unsigned long long* const buf1 = reinterpret_cast<unsigned long long*>(hist);  // hist + comb: idle now
+    bool cur = false;
+    for (int size = 2; size <= n2; size <<= 1) {
+        for (int stride2 = size >> 1; stride2 > 0; stride2 >>= 1) {
+            if (stride2 >= 128) {  // partners in other warps (block-uniform branch)
+                unsigned long long* const b = cur ? buf1 : sel;
+                if (holds) {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) b[4 * tid + u] = x[u];
+                }
+                __syncthreads();
+                if (holds) {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int i = 4 * tid + u, j = i ^ stride2;
+                        const unsigned long long y = b[j];
+                        const bool desc = (i & size) == 0, lower = i < j;
+                        x[u] = (desc == lower) ? (x[u] > y ? x[u] : y) : (x[u] < y ? x[u] : y);
+                    }
+                }
+                cur = !cur;
+            } else if (holds) {
                 if (stride2 >= 4) {  // partners in this warp: lane ^ (stride2 / 4)
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
                         const int i = 4 * tid + u, j = i ^ stride2;
                         const unsigned long long y = __shfl_xor_sync(0xffffffffu, x[u], stride2 >> 2);
-                        const bool desc = size == 128 || (i & size) == 0, lower = i < j;
+                        const bool desc = (i & size) == 0, lower = i < j;
                         x[u] = (desc == lower) ? (x[u] > y ? x[u] : y) : (x[u] < y ? x[u] : y);
                     }
                 } else {  // partners in this thread: (0, 2), (1, 3) for stride 2; (0, 1), (2, 3) for stride 1
                     auto cx = [&](unsigned long long& a, unsigned long long& b, int i) {  // i: a's index
-                        const bool desc = size == 128 || (i & size) == 0;
+                        const bool desc = (i & size) == 0;
                         if (desc ? (a < b) : (a > b)) { const unsigned long long t = a; a = b; b = t; }
                     };
                     if (stride2 == 2) { cx(x[0], x[2], 4 * tid); cx(x[1], x[3], 4 * tid + 1); }
@@ -447,40 +466,16 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreadsTopk)
             }
         }
     }
-    unsigned long long* src = sel;
-    unsigned long long* dst = reinterpret_cast<unsigned long long*>(hist);  // hist + comb: 64 KB, idle now
-#pragma unroll
-    for (int u = 0; u < 4; ++u)
-        if (holds) src[4 * tid + u] = x[u];
-    __syncthreads();
-    for (int len = 128; len < n2; len <<= 1) {
-        if (holds) {
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int i = 4 * tid + u;
-                const int list = i / len, off = i - list * len;
-                const unsigned long long* other = src + (list ^ 1) * len;
-                const bool first = (list & 1) == 0;
-                // number of the other list's items placed before x: greater than
-                // x, or equal to it when the other list is the first
-                int lo = 0, hi = len;
-                while (lo < hi) {
-                    const int mid = (lo + hi) >> 1;
-                    const unsigned long long o = other[mid];
-                    if (first ? (o > x[u]) : (o >= x[u])) lo = mid + 1; else hi = mid;
-                }
-                dst[(list & ~1) * len + off + lo] = x[u];
-            }
-        }
-        __syncthreads();
-        unsigned long long* t = src; src = dst; dst = t;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) x[u] = holds ? src[4 * tid + u] : 0ull;
-    }
-    sel = src;  // the sorted items
+    // the sorted items straight from registers: item i -> out[i]
     const int n_out = min(n_sel, k);
-    for (int i = tid; i < k; i += kThreadsTopk)
-        out[(int64_t)r * k + i] = i < n_out ? (int32_t)~(uint32_t)(sel[i] & 0xFFFFFFFFull) : -1;
+    if (holds) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int i = 4 * tid + u;
+            if (i < k) out[(int64_t)r * k + i] = i < n_out ? (int32_t)~(uint32_t)(x[u] & 0xFFFFFFFFull) : -1;
+        }
+    }
+    for (int i = n2 + tid; i < k; i += kThreadsTopk) out[(int64_t)r * k + i] = -1;
 }
 
 std::atomic<int> g_topk_attr[64];
