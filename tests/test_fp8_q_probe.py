@@ -4,7 +4,10 @@ summary part 2): q quantised to e4m3 with one UE8M0 scale per 32 dims (the
 block-scaled MMA's granularity), everything else exact, against the float64
 oracle with the exact q.  On the configured distribution the LSE moves far
 beyond the 1e-3 tolerance, so the decode keeps a bf16 QK; the probe records
-that decision with its numbers."""
+that decision with its numbers.  It also records the form that would keep the
+precision: q as the sum of two e4m3 parts with their own block scales (a bf16
+value has 8 significant bits, an e4m3 one 4), which gives the bf16 q back but
+for parts of a block that fall below the second part's range."""
 import math
 
 import numpy as np
@@ -37,7 +40,13 @@ def _quantise_q(q):
     return out
 
 
-def _probe(codes, seed):
+def _split_q(q):
+    """q as hi + lo, each e4m3 with one UE8M0 scale per 32 dims of its own."""
+    hi = _quantise_q(q)
+    return hi + _quantise_q(q - hi)
+
+
+def _probe(codes, seed, quantise=_quantise_q):
     rng = np.random.default_rng(seed)
     H, n = 16, 3000
     X = _entries(n, rng, codes)
@@ -45,7 +54,7 @@ def _probe(codes, seed):
     sink = rng.standard_normal(H)
     sm = 1 / math.sqrt(512)
     out, lse = O.decode_row(q, X, sink, sm)
-    out8, lse8 = O.decode_row(_quantise_q(q), X, sink, sm)
+    out8, lse8 = O.decode_row(quantise(q), X, sink, sm)
     return float(np.max(np.abs(lse8 - lse))), float(np.max(np.abs(out8 - out) / (1e-2 + 1e-2 * np.abs(out))))
 
 
@@ -59,3 +68,24 @@ def test_fp8_q_on_the_mild_distribution():
     dlse, dout = _probe(lambda n: np.full((n, 7), 127), 1)
     print(f"mild (all codes 127): max |dLSE| {dlse:.3g}, max out error / tolerance {dout:.3g}")
     assert dlse > 1e-3  # even logits of std ~1 move by more than the LSE tolerance
+
+
+def test_fp8_q_as_two_e4m3_parts_keeps_the_lse():
+    # configured: the two parts give every bf16 q value back (measured: 0);
+    # mild: a few small values of a block fall below the second part's
+    # subnormal range (measured: 1.7e-10)
+    for name, codes, seed in (("configured", lambda n: np.random.default_rng(1).integers(120, 135, size=(n, 7)), 0),
+                              ("mild", lambda n: np.full((n, 7), 127), 1)):
+        dlse, dout = _probe(codes, seed, quantise=_split_q)
+        print(f"{name}, q = hi + lo: max |dLSE| {dlse:.3g}, max out error / tolerance {dout:.3g}")
+        assert dlse <= 1e-6 and dout <= 1e-3
+
+
+def test_split_q_is_exact_for_bf16_values_in_range():
+    # a bf16 value is 8 significant bits: the e4m3 hi part takes the top 4 and
+    # the lo part the next 4 whenever both stay in their blocks' normal ranges
+    rng = np.random.default_rng(7)
+    q32 = rng.uniform(0.5, 1.0, (4, 64)).astype(np.float32)
+    q32[1] *= -3.0  # a block spanning two binades, scaled before rounding to bf16
+    q = torch.from_numpy(q32).to(torch.bfloat16).double().numpy()
+    assert np.array_equal(_split_q(q), q)
