@@ -1091,10 +1091,12 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, UnitDesc* units, in
             m_used = m_new;
             // A cold tile: for every head of this quarter, dropping the tile's
             // whole lo half keeps the skipped total within the budget on the bound
-            // alone (p <= 2^(mt_side - m) per entry, |lo| <= p 2^-9 by bf16
-            // rounding, and the new denominator is at least lsum alpha).  Then lo
-            // is not computed: it is stored as 0 and that bound stands in for its
-            // sum.  Both sides take the same decision from the same values.
+            // alone (p <= 2^(mt_side - m) per entry; p - bf16(p) is at most 2^-8 p,
+            // bf16's unit roundoff with 8 significant bits, and the stored lo at
+            // most (1 + 2^-8) times that; the new denominator is at least
+            // lsum alpha).  Then lo is not computed: it is stored as 0 and that
+            // bound stands in for its sum.  Both sides take the same decision from
+            // the same values.
             const uint32_t vb = c.sb + kOffXVmax + xs * (4 * kNumDequantWarps);
             float vmax = ld_shared_f32(vb);
 #pragma unroll
@@ -1106,7 +1108,7 @@ __device__ void softmax_role(const KParams& p, const Ctx& c, UnitDesc* units, in
                     pois |= ld_shared_u32(c.sb + kOffXPoison + (xs * kNumDequantWarps + w) * 4);
                 if (ok && ((pois >> sub) & 1u)) poisoned = true;
             }
-            const float capk = 32.f * (1.0f / 512.0f) * (1.0f + 1.0f / 256.0f);
+            const float capk = 32.f * (1.0f / 256.0f) * (1.0f + 1.0f / 256.0f);
             const float cap0 = mt0 == -INFINITY ? 0.f : capk * ex2_approx(mt0 - msub);
             const float cap1 = mt1 == -INFINITY ? 0.f : capk * ex2_approx(mt1 - msub);
             const bool cold = __all_sync(0xffffffffu, !live || (skipped * alpha + (cap0 + cap1) * vmax <= kLoBudget * lsum * alpha));
